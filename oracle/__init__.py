@@ -1,0 +1,227 @@
+"""Oracle for the MSA decode path — TEST INFRASTRUCTURE ONLY.
+
+Python access to ``msa_oracle.c``, a plain FP64 CPU restatement of what the
+MiniMax Sparse Attention decode path computes (index scan -> block max pool ->
+top-16 selection with the recent block kept -> exact softmax attention over the
+selected blocks' dequantised K/V). Only ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py`` may use it; the product path never
+does, and the oracle imports nothing from the product package.
+
+Inputs are duck-typed: any object with the workload attributes (``num_reqs``,
+``num_pages``, ``max_pages_per_req``, ``context_lens``, ``q_indptr``,
+``block_table``, ``q``, ``q_idx``, ``k_data``/``k_scale``, ``v_data``/``v_scale``,
+``ki_data``/``ki_scale``, ``sm_scale``, ``top_k``) as numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "msa_oracle.c")
+_LIB = os.path.join(_HERE, "libmsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+G, HQ, D, BLOCK = 4, 32, 128, 128
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (gcc, FP64, no FMA contraction so x86 and Arm agree)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + ".tmp"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                   check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [("num_reqs", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_pages_per_req", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("sm_scale", ctypes.c_double),
+                ("context_lens", ctypes.c_void_p), ("q_indptr", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("ki_data", ctypes.c_void_p), ("ki_scale", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int32)
+            ap = ctypes.POINTER(_Args)
+            lib.oracle_e2m1_value.restype = ctypes.c_double
+            lib.oracle_e2m1_value.argtypes = [ctypes.c_int]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_int]
+            lib.oracle_e4m3_round.restype = ctypes.c_int
+            lib.oracle_e4m3_round.argtypes = [ctypes.c_double]
+            lib.oracle_dequant_value.restype = ctypes.c_double
+            lib.oracle_dequant_value.argtypes = [ctypes.c_int, ctypes.c_int]
+            lib.oracle_dequant_table.argtypes = [dp]
+            lib.oracle_token_scores.argtypes = [ap, ctypes.c_int, dp]
+            lib.oracle_block_maxpool.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp]
+            lib.oracle_block_scores.argtypes = [ap, ctypes.c_int, dp]
+            lib.oracle_select.argtypes = [ctypes.c_int, ctypes.c_int, dp, ip]
+            lib.oracle_attend.argtypes = [ap, ctypes.c_int, ip, dp, dp]
+            lib.oracle_decode.argtypes = [ap, ctypes.c_int, ip, ip, dp, dp, dp]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            for f in ("oracle_token_scores", "oracle_block_maxpool", "oracle_block_scores", "oracle_select",
+                      "oracle_attend", "oracle_decode"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+class _Bound:
+    """Keeps the numpy arrays alive while the C struct points at them."""
+
+    def __init__(self, wl):
+        self.arrs = {
+            "context_lens": _c(wl.context_lens, np.int32), "q_indptr": _c(wl.q_indptr, np.int32),
+            "block_table": _c(wl.block_table, np.int32), "q": _c(wl.q, np.uint8), "q_idx": _c(wl.q_idx, np.uint8),
+            "k_data": _c(wl.k_data, np.uint8), "k_scale": _c(wl.k_scale, np.uint8),
+            "v_data": _c(wl.v_data, np.uint8), "v_scale": _c(wl.v_scale, np.uint8),
+            "ki_data": _c(wl.ki_data, np.uint8), "ki_scale": _c(wl.ki_scale, np.uint8),
+        }
+        self.args = _Args(num_reqs=int(wl.num_reqs), num_pages=int(wl.num_pages),
+                          max_pages_per_req=int(wl.max_pages_per_req), top_k=int(getattr(wl, "top_k", 16)),
+                          sm_scale=float(wl.sm_scale),
+                          **{k: v.ctypes.data for k, v in self.arrs.items()})
+
+    def ref(self):
+        return ctypes.byref(self.args)
+
+
+def _dp(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _ip(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+# ---- formats -----------------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e4m3_value(byte: int) -> float:
+    return _load().oracle_e4m3_value(int(byte))
+
+
+def e4m3_round(x: float) -> int:
+    return _load().oracle_e4m3_round(float(x))
+
+
+def dequant_value(code: int, scale: int) -> float:
+    return _load().oracle_dequant_value(int(code), int(scale))
+
+
+def dequant_table() -> np.ndarray:
+    """[256 scales, 16 codes] FP64 values the FP8 MMA consumes."""
+    out = np.empty(256 * 16, np.float64)
+    _load().oracle_dequant_table(_dp(out))
+    return out.reshape(256, 16)
+
+
+# ---- the path ----------------------------------------------------------------
+
+def _geom(wl, b):
+    N = int(wl.context_lens[b])
+    R = int(wl.q_indptr[b + 1] - wl.q_indptr[b])
+    return N, R
+
+
+def token_scores(wl, b: int) -> np.ndarray:
+    """Index scores of request b: [R, 4, N] FP64, -inf where a key lies after the row."""
+    N, R = _geom(wl, b)
+    out = np.empty(R * G * N + 1, np.float64)
+    bd = _Bound(wl)
+    _check(_load().oracle_token_scores(bd.ref(), b, _dp(out)), "token_scores")
+    return out[:R * G * N].reshape(R, G, N)
+
+
+def block_maxpool(token_s: np.ndarray) -> np.ndarray:
+    """[R, 4, N] token scores -> [4, nb] block scores (max over rows and block tokens)."""
+    R, g, N = token_s.shape
+    s = np.ascontiguousarray(token_s, dtype=np.float64)
+    nb = (N + BLOCK - 1) // BLOCK
+    out = np.empty(G * nb + 1, np.float64)
+    _check(_load().oracle_block_maxpool(R, N, _dp(s), _dp(out)), "block_maxpool")
+    return out[:G * nb].reshape(G, nb)
+
+
+def block_scores(wl, b: int) -> np.ndarray:
+    N, R = _geom(wl, b)
+    nb = (N + BLOCK - 1) // BLOCK
+    out = np.empty(G * nb + 1, np.float64)
+    bd = _Bound(wl)
+    _check(_load().oracle_block_scores(bd.ref(), b, _dp(out)), "block_scores")
+    return out[:G * nb].reshape(G, nb)
+
+
+def select(S_g: np.ndarray, top_k: int = 16) -> np.ndarray:
+    """Top-k block ids of one group's block scores (recent block kept), ascending, -1 padded."""
+    S = np.ascontiguousarray(S_g, dtype=np.float64)
+    ids = np.empty(top_k, np.int32)
+    _check(_load().oracle_select(len(S), top_k, _dp(S), _ip(ids)), "select")
+    return ids
+
+
+def attend(wl, b: int, ids: np.ndarray):
+    """Attention of request b over block ids [4, top_k]: (out [R,32,128], lse [R,32])."""
+    N, R = _geom(wl, b)
+    total = int(wl.total_rows)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    out = np.zeros((total, HQ, D), np.float64)
+    lse = np.zeros((total, HQ), np.float64)
+    bd = _Bound(wl)
+    _check(_load().oracle_attend(bd.ref(), b, _ip(ids), _dp(out), _dp(lse)), "attend")
+    r0 = int(wl.q_indptr[b])
+    return out[r0:r0 + R], lse[r0:r0 + R]
+
+
+def decode(wl, reqs=None):
+    """The whole path for the listed requests (all by default).
+
+    Returns dict(ids [n,4,top_k] int32, S [n,4,max_pages] FP64 block scores,
+    out [total_rows,32,128] FP64, lse [total_rows,32]) — rows of unlisted
+    requests stay zero."""
+    if reqs is None:
+        reqs = range(int(wl.num_reqs))
+    reqs = np.ascontiguousarray(np.asarray(list(reqs), dtype=np.int32))
+    n = len(reqs)
+    top_k = int(getattr(wl, "top_k", 16))
+    ids = np.empty((n, G, top_k), np.int32)
+    S = np.empty((n, G, int(wl.max_pages_per_req)), np.float64)
+    out = np.zeros((int(wl.total_rows), HQ, D), np.float64)
+    lse = np.zeros((int(wl.total_rows), HQ), np.float64)
+    bd = _Bound(wl)
+    _check(_load().oracle_decode(bd.ref(), n, _ip(reqs), _ip(ids), _dp(S), _dp(out), _dp(lse)), "decode")
+    return {"reqs": reqs, "ids": ids, "S": S, "out": out, "lse": lse}
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
