@@ -1,0 +1,385 @@
+// libmsa C ABI: argument validation, work planning, workspace layout and kernel
+// launches for the MSA decode path. The entry points and their contracts are
+// declared and documented in include/msa.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/msa.h"
+#include "msa_common.cuh"
+#include "msa_internal.h"
+
+namespace msa {
+
+namespace {
+
+constexpr size_t kWsAlign = 256;
+size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+int pow2_floor(int x) {
+  int p = 1;
+  while (p * 2 <= x) p *= 2;
+  return p;
+}
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int major = 0, minor = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+cudaError_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev & 63];
+  if (d.device != dev) {
+    int sms = 0, maj = 0, mi = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+    d.sm_count = sms;
+    d.major = maj;
+    d.minor = mi;
+    d.device = dev;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return cudaSuccess;
+}
+
+// 2-D view of an NVFP4 code plane [rows][64 bytes], boxes of 128 rows, 64-byte swizzle.
+msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows) {
+  if (get_encode_fn() != cudaSuccess) return MSA_ERR_CUDA;
+  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {64};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side checks of everything the host can see. Device-visible values
+// (lengths, page ids) are checked by the kernels.
+msa_status validate(const msa_decode_args* a, bool need_kv, bool need_idx) {
+  if (a == nullptr) return MSA_ERR_INVALID_ARG;
+  if (a->num_kv_heads != kGroups || a->q_per_kv != kQPerKV || a->head_dim != kDim || a->block_size != kBlock ||
+      a->top_k != kTopK)
+    return MSA_ERR_UNSUPPORTED;
+  if (a->num_reqs < 0 || a->num_reqs > kMaxReqs || a->total_rows < 0 || a->max_rows_per_req < 1 ||
+      a->max_rows_per_req > kMaxRows || a->num_pages < 1 || a->max_pages_per_req < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(a->total_rows) > static_cast<long long>(a->num_reqs) * a->max_rows_per_req)
+    return MSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(a->num_pages) * kGroups * kBlock >= (1LL << 31)) return MSA_ERR_UNSUPPORTED;
+  if (!(a->sm_scale > 0.f) || !std::isfinite(a->sm_scale)) return MSA_ERR_INVALID_ARG;
+  if (a->num_reqs > 0 && (a->context_lens == nullptr || a->q_indptr == nullptr || a->block_table == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  const bool rows = a->total_rows > 0;
+  if (need_idx && ((rows && a->q_idx == nullptr) || a->ki_data == nullptr || a->ki_scale == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (need_kv && ((rows && a->q == nullptr) || a->k_data == nullptr || a->k_scale == nullptr || a->v_data == nullptr ||
+                  a->v_scale == nullptr))
+    return MSA_ERR_INVALID_ARG;
+  if (need_idx && (!aligned16(a->q_idx) || !aligned16(a->ki_data) || !aligned16(a->ki_scale)))
+    return MSA_ERR_INVALID_ARG;
+  if (need_kv && (!aligned16(a->q) || !aligned16(a->k_data) || !aligned16(a->k_scale) || !aligned16(a->v_data) ||
+                  !aligned16(a->v_scale)))
+    return MSA_ERR_INVALID_ARG;
+  return MSA_OK;
+}
+
+msa_status check_device(DeviceInfo* d) {
+  if (device_info(d) != cudaSuccess) return MSA_ERR_CUDA;
+  if (d->major != 10 || d->minor != 3) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+struct Ws {
+  uint32_t* flags;
+  uint32_t* req_cnt;
+  uint32_t* pair_cnt;
+  float* block_S;
+  float* part_o;
+  float* part_lse2;
+};
+
+msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, const Plan& plan, Ws* w) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return MSA_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(a->num_reqs, a->total_rows, a->max_rows_per_req, a->max_pages_per_req, plan);
+  if (ws_bytes < L.total) return MSA_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  w->flags = reinterpret_cast<uint32_t*>(base + L.flags);
+  w->req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
+  w->pair_cnt = reinterpret_cast<uint32_t*>(base + L.pair_cnt);
+  w->block_S = reinterpret_cast<float*>(base + L.block_S);
+  w->part_o = reinterpret_cast<float*>(base + L.part_o);
+  w->part_lse2 = reinterpret_cast<float*>(base + L.part_lse2);
+  return MSA_OK;
+}
+
+SelectParams select_params(const msa_decode_args* a, const Ws& w, int32_t* ids, float* scores_out) {
+  SelectParams p = {};
+  p.num_reqs = a->num_reqs;
+  p.num_pages = a->num_pages;
+  p.max_pages = a->max_pages_per_req;
+  p.total_rows = a->total_rows;
+  p.context_lens = a->context_lens;
+  p.q_indptr = a->q_indptr;
+  p.block_table = a->block_table;
+  p.q_idx = a->q_idx;
+  p.ki_scale = a->ki_scale;
+  p.block_S = w.block_S;
+  p.req_cnt = w.req_cnt;
+  p.flags = w.flags;
+  p.block_ids = ids;
+  p.block_scores_out = scores_out;
+  return p;
+}
+
+AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, const int32_t* ids, uint16_t* out,
+                       float* lse) {
+  AttnParams p = {};
+  p.num_reqs = a->num_reqs;
+  p.num_pages = a->num_pages;
+  p.max_pages = a->max_pages_per_req;
+  p.total_rows = a->total_rows;
+  p.context_lens = a->context_lens;
+  p.q_indptr = a->q_indptr;
+  p.block_table = a->block_table;
+  p.block_ids = ids;
+  p.q = a->q;
+  p.k_data = a->k_data;
+  p.k_scale = a->k_scale;
+  p.v_data = a->v_data;
+  p.v_scale = a->v_scale;
+  p.sm_scale_log2 = a->sm_scale * 1.4426950408889634f;
+  p.blocks_per_split = plan.blocks_per_split;
+  p.splits = plan.splits;
+  p.max_m = kQPerKV * a->max_rows_per_req;
+  p.part_o = w.part_o;
+  p.part_lse2 = w.part_lse2;
+  p.pair_cnt = w.pair_cnt;
+  p.flags = w.flags;
+  p.out = out;
+  p.lse = lse;
+  return p;
+}
+
+}  // namespace
+
+Plan make_plan(int num_reqs, int sm_count) {
+  Plan pl;
+  pl.select_grid = 2 * sm_count;  // two resident CTAs per SM (tensor memory: 256 columns each)
+  const int pairs = num_reqs * kGroups;
+  const int target = 2 * sm_count;
+  int bps = pairs > 0 ? pow2_floor((kTopK * pairs) / target) : kTopK;
+  if (bps < 1) bps = 1;
+  if (bps > kTopK) bps = kTopK;
+  pl.blocks_per_split = bps;
+  pl.splits = kTopK / bps;
+  return pl;
+}
+
+WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan) {
+  WsLayout L;
+  (void)total_rows;
+  size_t off = 0;
+  L.flags = off;
+  off = align_up(off + 16);
+  L.req_cnt = off;
+  off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs));
+  L.pair_cnt = off;
+  off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs) * kGroups);
+  L.block_S = off;
+  off = align_up(off + sizeof(float) * 4 * static_cast<size_t>(num_reqs) * kGroups * max_pages);
+  const size_t m = static_cast<size_t>(kQPerKV) * max_rows_per_req;
+  const size_t parts = plan.splits > 1 ? static_cast<size_t>(plan.splits) * num_reqs * kGroups * m : 0;
+  L.part_o = off;
+  off = align_up(off + sizeof(float) * parts * kDim);
+  L.part_lse2 = off;
+  off = align_up(off + sizeof(float) * parts);
+  L.total = off;
+  return L;
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+const char* msa_status_string(msa_status s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported geometry or device";
+    case MSA_ERR_CUDA: return "CUDA runtime error";
+    case MSA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case MSA_ERR_BAD_TABLE: return "out-of-range page id or length seen on the device";
+    case MSA_ERR_TIMEOUT: return "a bounded on-chip wait timed out";
+  }
+  return "unknown status";
+}
+
+msa_status msa_workspace_size(const msa_decode_args* args, size_t* bytes) {
+  if (bytes == nullptr) return MSA_ERR_INVALID_ARG;
+  msa_status st = validate(args, false, false);
+  if (st != MSA_OK) return st;
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return MSA_ERR_CUDA;
+  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  *bytes = ws_layout(args->num_reqs, args->total_rows, args->max_rows_per_req, args->max_pages_per_req, plan).total;
+  return MSA_OK;
+}
+
+msa_status msa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return MSA_ERR_WORKSPACE;
+  return cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_get_error(void* ws, size_t ws_bytes, void* stream, uint32_t* flags) {
+  if (ws == nullptr || ws_bytes < 16 || flags == nullptr) return MSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (h != 0 && cudaMemsetAsync(ws, 0, sizeof(h), st) != cudaSuccess) return MSA_ERR_CUDA;
+  *flags = h;
+  if (h & MSA_FLAG_TIMEOUT) return MSA_ERR_TIMEOUT;
+  if (h != 0) return MSA_ERR_BAD_TABLE;
+  return MSA_OK;
+}
+
+static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
+                             long long stride, void* ws, size_t ws_bytes, cudaStream_t st) {
+  DeviceInfo d;
+  msa_status s = check_device(&d);
+  if (s != MSA_OK) return s;
+  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if (args->num_reqs == 0) return MSA_OK;
+  CUtensorMap map;
+  if ((s = encode_code_map(&map, args->ki_data, static_cast<long long>(args->num_pages) * kBlock)) != MSA_OK) return s;
+  SelectParams p = select_params(args, w, ids, scores_out);
+  p.token_scores = tok;
+  p.score_stride = stride;
+  return launch_select(map, p, mode, plan.select_grid, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_index_scores(const msa_decode_args* args, float* scores, int64_t score_stride, void* ws,
+                            size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, false, true);
+  if (s != MSA_OK) return s;
+  if (scores == nullptr || score_stride < static_cast<int64_t>(args->max_pages_per_req) * kBlock)
+    return MSA_ERR_INVALID_ARG;
+  return run_select(args, 1, nullptr, nullptr, scores, score_stride, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, float* block_scores, void* ws,
+                             size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, false, true);
+  if (s != MSA_OK) return s;
+  if (block_ids == nullptr) return MSA_ERR_INVALID_ARG;
+  return run_select(args, 0, block_ids, block_scores, nullptr, 0, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scores, int64_t score_stride,
+                                  int32_t* block_ids, float* block_scores, void* ws, size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, false, false);
+  if (s != MSA_OK) return s;
+  if (scores == nullptr || block_ids == nullptr ||
+      score_stride < static_cast<int64_t>(args->max_pages_per_req) * kBlock)
+    return MSA_ERR_INVALID_ARG;
+  DeviceInfo d;
+  if ((s = check_device(&d)) != MSA_OK) return s;
+  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if (args->num_reqs == 0) return MSA_OK;
+  MaxpoolParams p = {};
+  p.num_reqs = args->num_reqs;
+  p.max_pages = args->max_pages_per_req;
+  p.total_rows = args->total_rows;
+  p.context_lens = args->context_lens;
+  p.q_indptr = args->q_indptr;
+  p.scores = scores;
+  p.score_stride = score_stride;
+  p.block_S = w.block_S;
+  p.block_ids = block_ids;
+  p.block_scores_out = block_scores;
+  p.flags = w.flags;
+  return launch_maxpool_topk(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+static msa_status run_attn(const msa_decode_args* args, const int32_t* ids, uint16_t* out, float* lse, void* ws,
+                           size_t ws_bytes, cudaStream_t st, bool pdl) {
+  DeviceInfo d;
+  msa_status s = check_device(&d);
+  if (s != MSA_OK) return s;
+  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if (args->num_reqs == 0) return MSA_OK;
+  AttnParams p = attn_params(args, w, plan, ids, out, lse);
+  return launch_attn(p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* block_ids, uint16_t* out_bf16,
+                                  float* lse, void* ws, size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, true, false);
+  if (s != MSA_OK) return s;
+  if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
+  return run_attn(args, block_ids, out_bf16, lse, ws, ws_bytes, static_cast<cudaStream_t>(stream), false);
+}
+
+msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, true, true);
+  if (s != MSA_OK) return s;
+  if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((s = run_select(args, 0, block_ids, nullptr, nullptr, 0, ws, ws_bytes, st)) != MSA_OK) return s;
+  return run_attn(args, block_ids, out_bf16, lse, ws, ws_bytes, st, true);
+}
+
+msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t nrows, uint8_t* out_e4m3,
+                            int32_t path, void* stream) {
+  if (codes == nullptr || scales == nullptr || out_e4m3 == nullptr || nrows < 0 || (path != 0 && path != 1))
+    return MSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(codes) & 3u) != 0 || (reinterpret_cast<uintptr_t>(out_e4m3) & 3u) != 0)
+    return MSA_ERR_INVALID_ARG;
+  DeviceInfo d;
+  msa_status s = check_device(&d);
+  if (s != MSA_OK) return s;
+  if (nrows == 0) return MSA_OK;
+  return launch_dequant_rows(codes, scales, nrows, out_e4m3, path, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MSA_OK
+             : MSA_ERR_CUDA;
+}
+
+}  // extern "C"

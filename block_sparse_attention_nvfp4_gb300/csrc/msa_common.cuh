@@ -1,0 +1,335 @@
+// Device-side building blocks shared by the libmsa kernels: constants, the
+// workspace layout, bounded mbarrier waits, TMA / bulk-copy issue, tcgen05
+// (TMEM) wrappers, the NVFP4 -> E4M3 dequantisers and the warp top-k.
+//
+// Sources for the method (cited by tag):
+//   [vLLM-zh] vLLM day-0 blog post on MiniMax-M3.1-Flash (Chinese rewrite,
+//             agentlenshq.com): "How MiniMax sparse attention works", "Blackwell
+//             MSA kernels / dequantising NVFP4 to FP8 with QMUL4", "AMD NVFP4
+//             MSA kernel via table lookup".
+//   [MSA-fig] "MiniMax goes sparse: reading the M3 attention mechanism from one
+//             diagram" (atlascloud.ai), section 1.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+constexpr int kGroups = 4;        // KV heads = GQA groups
+constexpr int kHeads = 32;        // query heads
+constexpr int kQPerKV = 8;
+constexpr int kDim = 128;
+constexpr int kBlock = 128;       // tokens per page / KV block
+constexpr int kTopK = 16;
+constexpr int kMaxRows = 8;       // query rows per request (speculative decode)
+constexpr int kMaxReqs = 4096;      // per-request tables live in shared memory
+
+// device error flags (match MSA_FLAG_* in msa.h)
+constexpr uint32_t kFlagBadPage = 0x1u;
+constexpr uint32_t kFlagBadLength = 0x2u;
+constexpr uint32_t kFlagTimeout = 0x4u;
+constexpr uint32_t kFlagBadIds = 0x8u;
+
+// bounded waits give up after this long (ns of %globaltimer)
+constexpr long long kWaitLimitNs = 1000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_flag(uint32_t* flags, uint32_t f) { atomicOr(flags, f); }
+
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(bar), "r"(tx)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
+// On timeout sets the timeout flag and returns false.
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* flags) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = global_ns();
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      set_flag(flags, kFlagTimeout);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- async copies
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- PDL
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------- tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane <- v[0..15]
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// v[0..31] <- 32 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1u) << 16;                 // leading byte offset (unused when swizzled)
+  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;  // stride byte offset: next 8-row group
+  d |= static_cast<uint64_t>(1u) << 46;                 // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> F32, K-major A and B.
+__device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N, bool negate_b) {
+  return (1u << 4) | (negate_b ? (1u << 14) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D[tmem] (+)= A[tmem] x B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_f8_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p; }" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------- warp MMA (legacy path)
+// D(16x8, f32) += A(16x32, e4m3) * B(32x8, e4m3)
+__device__ __forceinline__ void mma_m16n8k32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- NVFP4 -> E4M3
+// [vLLM-zh, Blackwell kernels] the cache is NVFP4 while queries are FP8, so the
+// kernels turn NVFP4 into FP8 before an FP8 MMA. The FP8 value of an element is
+// its E2M1 value times its E4M3 group scale, rounded to E4M3. With 256 possible
+// scales and 8 E2M1 magnitudes that is a table ([vLLM-zh, AMD NVFP4 MSA kernel
+// via table lookup]: 256 scales x 8 magnitudes, pre-rounded to FP8). Here each
+// CTA builds it in shared memory with the hardware conversions and byte-permute
+// instructions do four lookups at a time.
+//
+// Entry for scale s (16 bytes): x,y = magnitude bytes |E4M3(m_c * s)| for
+// c = 0..7; z,w = the same bytes in reverse order (index 7-c).
+struct LutEntry {
+  uint32_t p0, p1, n0, n1;
+};
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2_scaled(uint32_t byte_pair, uint32_t scale_h2) {
+  uint32_t h;
+  uint16_t e;
+  asm("{ .reg .b8 b; cvt.u8.u32 b, %1; cvt.rn.f16x2.e2m1x2 %0, b; }" : "=r"(h) : "r"(byte_pair));
+  asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(scale_h2));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(e) : "r"(h));
+  return e;
+}
+__device__ __forceinline__ uint32_t e4m3_to_h2_bcast(uint32_t sbyte) {
+  uint32_t h;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "r"(sbyte));
+  return (h & 0xFFFFu) | (h << 16);
+}
+// One entry per thread of the block; 256 entries.
+__device__ __forceinline__ void build_lut(LutEntry* lut) {
+  for (int s = threadIdx.x; s < 256; s += blockDim.x) {
+    // magnitudes of E2M1 codes 0..7 (the e2m1x2 conversions take code pairs)
+    const uint32_t sc = e4m3_to_h2_bcast(static_cast<uint32_t>(s & 0x7F));
+    const uint32_t lo = cvt_e2m1x2_scaled(0x10, sc) | (cvt_e2m1x2_scaled(0x32, sc) << 16);
+    const uint32_t hi = cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16);
+    LutEntry e;
+    e.p0 = lo;
+    e.p1 = hi;
+    e.n0 = __byte_perm(hi, 0, 0x0123);
+    e.n1 = __byte_perm(lo, 0, 0x0123);
+    lut[s] = e;
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Signed form: 8 elements of code word w (element k in nibble k) -> two words of
+// E4M3 bytes, r0 = elements 0..3, r1 = elements 4..7. Magnitudes come from the
+// scale's entry (selector bit 3 cleared); the sign of nibble k lands on bit 7 of
+// output byte k.
+__device__ __forceinline__ void dq8_signed(uint32_t w, uint32_t L0, uint32_t L1, uint32_t& r0, uint32_t& r1) {
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t m0 = prmt(L0, L1, sel);
+  const uint32_t m1 = prmt(L0, L1, sel >> 16);
+  const uint32_t u = w << 4;
+  const uint32_t s0 = prmt(w, u, 0x1504);  // byte k's msb = sign of nibble k, k = 0..3
+  const uint32_t s1 = prmt(w, u, 0x3726);  // nibbles 4..7
+  r0 = m0 ^ (s0 & 0x80808080u);
+  r1 = m1 ^ (s1 & 0x80808080u);
+}
+
+// Split form for the index scan: positive-part bytes p (magnitude where the
+// element is positive, 0 where negative) and negative-part bytes n (magnitude
+// where negative, 0 where positive), so k = p - n elementwise. The byte permute
+// in its default mode turns a selector nibble with bit 3 set into the sign
+// replicate of the chosen byte, which is 0 for these (non-negative) table bytes:
+// the raw code nibble picks the magnitude of positive elements and zeroes
+// negative ones; the complemented nibble (sign flipped, index 7-c into the
+// reversed table) does the opposite. The MMA then subtracts the n part by
+// negating its B operand.
+__device__ __forceinline__ void dq8_split(uint32_t w, const LutEntry& L, uint32_t& p0, uint32_t& p1, uint32_t& n0,
+                                          uint32_t& n1) {
+  const uint32_t wh = w >> 16;
+  p0 = prmt(L.p0, L.p1, w);
+  p1 = prmt(L.p0, L.p1, wh);
+  n0 = prmt(L.n0, L.n1, ~w);
+  n1 = prmt(L.n0, L.n1, ~wh);
+}
+
+// ---------------------------------------------------------------- top-k
+// [vLLM-zh §How; MSA-fig §1 TopK] One warp selects the blocks of one group:
+// the most recent block (nb-1) plus the 15 best of blocks 0..nb-2 by score,
+// ties to the lower id; every block when nb <= 16. ids_out gets 16 ascending
+// ids, -1 padded. S is read with plain loads (written by this or other CTAs
+// before a device-scope fence). fmaxf ignores a NaN partial; a block whose
+// partials are all NaN ranks last.
+__device__ __forceinline__ uint64_t topk_key(float v, int id) {
+  uint32_t u = __float_as_uint(v);
+  uint32_t hi;
+  if (v != v) hi = 0u;                       // NaN ranks below everything
+  else hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(hi) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+
+__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+
+// S[c] holds partial maxima of block c (their max is the block score).
+static __device__ __noinline__ void warp_topk(const float4* S, int nb, int32_t* ids_out) {
+  const int lane = threadIdx.x & 31;
+  if (nb <= kTopK) {
+    if (lane < kTopK) ids_out[lane] = lane < nb ? lane : -1;
+    return;
+  }
+  constexpr int L = kTopK - 1;
+  uint64_t list[L];
+#pragma unroll
+  for (int j = 0; j < L; ++j) list[j] = 0ull;
+  for (int c = lane; c < nb - 1; c += 32) {
+    const uint64_t key = topk_key(max4(S[c]), c);
+    if (key > list[L - 1]) {
+#pragma unroll
+      for (int j = L - 1; j > 0; --j) list[j] = (key > list[j - 1]) ? list[j - 1] : ((key > list[j]) ? key : list[j]);
+      list[0] = key > list[0] ? key : list[0];
+    }
+  }
+  int my_id = nb - 1;  // lane 15 keeps the recent block
+#pragma unroll 1
+  for (int k = 0; k < L; ++k) {
+    uint64_t best = list[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(best), off);
+      const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(best >> 32), off);
+      const uint64_t o = (static_cast<uint64_t>(hi) << 32) | lo;
+      best = o > best ? o : best;
+    }
+    if (list[0] == best) {  // keys are unique per block id: exactly one lane
+#pragma unroll
+      for (int j = 0; j < L - 1; ++j) list[j] = list[j + 1];
+      list[L - 1] = 0ull;
+    }
+    if (lane == k) my_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+  }
+  // ascending order: rank among lanes 0..15
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const int other = __shfl_sync(0xFFFFFFFFu, my_id, j);
+    rank += (other < my_id) ? 1 : 0;
+  }
+  if (lane < kTopK) ids_out[rank] = my_id;
+}
+
+}  // namespace msa

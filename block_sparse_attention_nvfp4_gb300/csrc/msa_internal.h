@@ -1,0 +1,86 @@
+// Host/device interface between libmsa's C ABI (msa_api.cu) and its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msa {
+
+// Fused index scan -> block max pool -> top-k (and the per-token score variant).
+struct SelectParams {
+  int num_reqs, num_pages, max_pages, total_rows;
+  const int32_t* context_lens;
+  const int32_t* q_indptr;
+  const int32_t* block_table;
+  const uint8_t* q_idx;
+  const uint8_t* ki_scale;
+  float* block_S;           // workspace [B][4][max_pages][4 partials]
+  uint32_t* req_cnt;        // workspace [B] arrival counters
+  uint32_t* flags;          // workspace error flags
+  int32_t* block_ids;       // [B][4][16]
+  float* block_scores_out;  // optional [B][4][max_pages]
+  float* token_scores;      // per-token variant: [rows][4][score_stride]
+  long long score_stride;
+};
+
+struct MaxpoolParams {
+  int num_reqs, max_pages, total_rows;
+  const int32_t* context_lens;
+  const int32_t* q_indptr;
+  const float* scores;
+  long long score_stride;
+  float* block_S;
+  int32_t* block_ids;
+  float* block_scores_out;
+  uint32_t* flags;
+};
+
+// Sparse attention over selected blocks, split across CTAs, merged by the last arriver.
+struct AttnParams {
+  int num_reqs, num_pages, max_pages, total_rows;
+  const int32_t* context_lens;
+  const int32_t* q_indptr;
+  const int32_t* block_table;
+  const int32_t* block_ids;  // [B][4][16]
+  const uint8_t* q;
+  const uint8_t* k_data;
+  const uint8_t* k_scale;
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  float sm_scale_log2;       // sm_scale * log2(e)
+  int blocks_per_split;
+  int splits;
+  int max_m;                 // 8 * max_rows_per_req
+  float* part_o;             // workspace [splits][B*4][max_m][128]
+  float* part_lse2;          // workspace [splits][B*4][max_m] (log2 domain)
+  uint32_t* pair_cnt;        // workspace [B*4]
+  uint32_t* flags;
+  uint16_t* out;             // [rows][32][128] bf16 bits
+  float* lse;                // optional [rows][32]
+};
+
+// Workspace layout, offsets in bytes (each 256-aligned).
+struct WsLayout {
+  size_t flags, req_cnt, pair_cnt, block_S, part_o, part_lse2, total;
+};
+
+struct Plan {
+  int select_grid;        // CTAs of the scan kernel
+  int blocks_per_split;   // attention
+  int splits;
+};
+
+Plan make_plan(int num_reqs, int sm_count);
+WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan);
+
+size_t select_smem_bytes(int num_reqs);
+size_t attn_smem_bytes();
+cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int grid, cudaStream_t st);
+cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
+cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
+cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,
+                                cudaStream_t st);
+
+}  // namespace msa

@@ -1,0 +1,179 @@
+/*
+ * libmsa — the decode hot path of MiniMax Sparse Attention (MSA) over an NVFP4
+ * paged KV cache, as CUDA kernels for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited below by the tag in brackets):
+ *   [vLLM-zh]  "vLLM 对 MiniMax-M3.1-Flash 的 Day-0 支持：NVFP4 MSA 内核、MegaMoE 与
+ *              Agentic 基准测试" (agentlenshq.com): the vLLM day-0 blog post on
+ *              MiniMax-M3.1-Flash, Chinese rewrite. Sections used: "How MiniMax
+ *              sparse attention works", "Blackwell MSA kernels / dequantising NVFP4
+ *              to FP8 with the CUDA 13.4 QMUL4 instruction", "NVFP4 indexer decode
+ *              context parallelism", "Rubin MSA kernels".
+ *   [MSA-fig]  "MiniMax goes sparse: reading the M3 attention mechanism from one
+ *              diagram" (atlascloud.ai), section 1: the index branch (shared
+ *              single-head K_idx, block max pool, top-k) and the sparse branch.
+ *
+ * What the path computes, per request b with N context tokens (including this
+ * step's R query rows, which sit at positions N-R .. N-1 and see keys t <= their
+ * own position):
+ *   1. index scan   s[r][g][t] = q_idx[r][g] . k_idx[t]   for every context token
+ *                   (one FP8 index query per GQA group against one shared NVFP4
+ *                   index-key head, dequantised to FP8)           [vLLM-zh §How]
+ *   2. block pool   S[g][c] = max over rows r and tokens t of block c  [vLLM-zh §How]
+ *   3. top-k        16 blocks per group: the most recent block plus the 15 best
+ *                   others (ties to the lower block id); all blocks if <= 16
+ *                                                        [vLLM-zh §How; MSA-fig §1]
+ *   4. attention    softmax((q . k) * sm_scale) V over the selected blocks' keys,
+ *                   K/V dequantised from NVFP4 to FP8, every query head of the
+ *                   group sharing the group's selection   [vLLM-zh §How; MSA-fig §1]
+ *
+ * Geometry: 4 KV heads (GQA groups) x head dim 128, 8 query heads per KV head,
+ * one shared index-key head of dim 128, 128-token pages (= KV blocks), top_k 16.
+ * Other values return MSA_ERR_UNSUPPORTED.
+ *
+ * Formats. FP8 = OCP E4M3 ("FN": no infinities, S.1111.111 = NaN, max 448).
+ * NVFP4 = E2M1 element codes with one E4M3 scale per 16 consecutive elements; a
+ * 128-element row is 64 code bytes (element 2i in the low nibble of byte i) plus
+ * 8 scale bytes. Scale bytes of written slots must be non-negative (sign bit
+ * clear), as NVFP4 scales are amax/6. The dequantised value is the E2M1 value
+ * times its scale, rounded to E4M3 (nearest, ties to even, saturating) — the FP8
+ * value an FP8 MMA consumes ([vLLM-zh] Blackwell and Rubin kernel sections).
+ *
+ * Cache layout (data and scale planes separate; P = num_pages):
+ *   k_data, v_data   [P][4][128][64]   k_scale, v_scale   [P][4][128][8]
+ *   ki_data          [P][128][64]      ki_scale           [P][128][8]
+ * Slots of a page beyond a request's context may hold anything; they are never
+ * used. Every cache pointer must be 16-byte aligned.
+ *
+ * Ownership and execution. Every pointer in msa_decode_args and every buffer
+ * argument is a DEVICE pointer owned by the caller (unless marked host). Calls
+ * enqueue work on `stream` (a cudaStream_t; NULL = legacy default stream),
+ * never synchronise (except msa_get_error) and never allocate device memory.
+ * Arguments are validated on the host before any launch; a failed check
+ * returns an error and launches nothing. Values only the device can see (page
+ * ids, context lengths, row counts) are checked by the kernels: a bad value sets
+ * a flag in the workspace, the affected work is skipped, and msa_get_error
+ * reports it. No call raises a device-side trap.
+ *
+ * Workspace. `ws` is caller-owned device memory of at least msa_workspace_size()
+ * bytes, 256-byte aligned, zero-filled once before first use (msa_workspace_init).
+ * The kernels leave its counters at zero when they finish, so one workspace
+ * serves any number of successive calls on one stream; calls running at the
+ * same time need separate workspaces.
+ */
+#ifndef LIBMSA_MSA_H_
+#define LIBMSA_MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = -1,   /* a host-checkable argument is out of range or NULL */
+  MSA_ERR_UNSUPPORTED = -2,   /* geometry other than 4 x 8 x 128, block 128, top-k 16; device not sm_103 */
+  MSA_ERR_CUDA = -3,          /* a CUDA runtime call failed (launch, attribute, ...) */
+  MSA_ERR_WORKSPACE = -4,     /* workspace NULL, too small or misaligned */
+  MSA_ERR_BAD_TABLE = -5,     /* (msa_get_error) a page id or length seen on the device was out of range */
+  MSA_ERR_TIMEOUT = -6        /* (msa_get_error) a bounded on-chip wait gave up */
+} msa_status;
+
+/* Device error flags reported by msa_get_error (bitwise OR). */
+#define MSA_FLAG_BAD_PAGE    0x1u   /* block_table entry outside [0, num_pages) */
+#define MSA_FLAG_BAD_LENGTH  0x2u   /* context_lens / q_indptr inconsistent with the limits */
+#define MSA_FLAG_TIMEOUT     0x4u   /* an mbarrier / async-copy wait hit its time limit */
+#define MSA_FLAG_BAD_IDS     0x8u   /* msa_sparse_attn_decode got a block id outside the context */
+
+typedef struct {
+  int32_t num_reqs;            /* B >= 0 */
+  int32_t total_rows;          /* query rows this step = q_indptr[B] (host copy of the value) */
+  int32_t max_rows_per_req;    /* upper bound on any request's rows, 1..8 */
+  int32_t num_pages;           /* P, physical pages in each cache */
+  int32_t max_pages_per_req;   /* row length of block_table; context_lens[b] <= 128 * this */
+  int32_t num_kv_heads;        /* 4 */
+  int32_t q_per_kv;            /* 8 */
+  int32_t head_dim;            /* 128 */
+  int32_t block_size;          /* 128 */
+  int32_t top_k;               /* 16 */
+  float sm_scale;              /* attention logit scale, usually 1/sqrt(128) */
+  const int32_t* context_lens; /* [B] tokens in the cache including this step's rows */
+  const int32_t* q_indptr;     /* [B+1] request b owns rows [q_indptr[b], q_indptr[b+1]) */
+  const int32_t* block_table;  /* [B][max_pages_per_req] physical page of logical block c */
+  const uint8_t* q;            /* [total_rows][32][128] E4M3 queries; head h uses KV head h/8 */
+  const uint8_t* q_idx;        /* [total_rows][4][128] E4M3 index queries, one per group */
+  const uint8_t* k_data;       /* NVFP4 caches, layouts above */
+  const uint8_t* k_scale;
+  const uint8_t* v_data;
+  const uint8_t* v_scale;
+  const uint8_t* ki_data;
+  const uint8_t* ki_scale;
+} msa_decode_args;
+
+/* Static text for a status code. */
+const char* msa_status_string(msa_status status);
+
+/* Bytes of workspace the calls below need for `args` on the current device
+ * (depends on num_reqs, total_rows, max_rows_per_req, max_pages_per_req and
+ * the SM count). Writes *bytes; host-only, no launch. */
+msa_status msa_workspace_size(const msa_decode_args* args, size_t* bytes);
+
+/* Zero-fill a workspace (async memset on `stream`). Needed once per workspace. */
+msa_status msa_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Read and clear the device error flags in `ws` (synchronises `stream`).
+ * *flags (host) receives MSA_FLAG_* bits; returns MSA_OK when none is set,
+ * else the matching error code. */
+msa_status msa_get_error(void* ws, size_t ws_bytes, void* stream, uint32_t* flags);
+
+/* Step 1 alone (debug / unfused path) [vLLM-zh §How; MSA-fig §1 step 1].
+ * scores[(row * 4 + g) * score_stride + t] = q_idx[row][g] . k_idx(request, t)
+ * for t < context length (FP32, FP8 x FP8 products summed in FP32); -inf where
+ * t is after the row's position. score_stride >= max context length (elements);
+ * entries at t >= context length are left unwritten. */
+msa_status msa_index_scores(const msa_decode_args* args, float* scores, int64_t score_stride,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 2+3 from given token scores laid out as msa_index_scores writes them
+ * [vLLM-zh §How; MSA-fig §1 "Block Max Pool", "TopK"]. Writes block_ids
+ * [B][4][16] (int32, ascending, -1 padded) and, if block_scores is not NULL,
+ * block_scores[B][4][max_pages_per_req] (FP32 block maxima, -inf past the
+ * context). Ties between equal block scores go to the lower block id. */
+msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scores, int64_t score_stride,
+                                  int32_t* block_ids, float* block_scores,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 1+2+3 fused: one streaming pass over the index-key cache with the block
+ * max pool and the top-k in its epilogue; per-token scores never reach memory.
+ * Outputs as msa_block_maxpool_topk. This is the first kernel of msa_decode. */
+msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4 given block ids [B][4][16] (ascending or not, -1 = unused)
+ * [vLLM-zh §How; MSA-fig §1 step 2]. out_bf16[row][32][128] (BF16 bits) gets
+ * softmax attention over the keys of the listed blocks visible to the row; lse
+ * (optional, [total_rows][32] FP32) gets log(sum(exp(logits))), natural log. */
+msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* block_ids,
+                                  uint16_t* out_bf16, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, the
+ * second launch chained to the first with programmatic dependent launch. */
+msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* The dequantisers the kernels use, exposed for checking: rows of 128 NVFP4
+ * elements (codes [n][64], scales [n][8]) -> E4M3 bytes out_e4m3 [n][128], element
+ * j of row i at out_e4m3[i*128 + j]. path 0 = the signed form the attention
+ * kernel feeds its MMA; path 1 = the index scan's form, which splits each row
+ * into positive and negative magnitude parts (recombined here into one signed
+ * byte; a zero may come back as either sign).
+ * [vLLM-zh, Blackwell kernels: NVFP4 turned into FP8 before the FP8 MMA] */
+msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t nrows,
+                            uint8_t* out_e4m3, int32_t path, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIBMSA_MSA_H_ */

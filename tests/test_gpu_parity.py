@@ -1,0 +1,188 @@
+"""GPU parity: libmsa through its C ABI against the oracle on seeded inputs.
+
+Acceptance rules: block ids bit-exact except where the oracle's 16th and 17th
+block scores are within 1e-4 relative (a near-tie the FP32 sums may break either
+way); outputs |gpu - oracle| <= 2e-2 + 2e-2 |oracle|; index scores within the
+FP32 summation bound of 128 exact products (<= 8e-6 * sum|q_j k_j|); integer work
+on identical inputs (max pool + top-k from given scores) bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_nvfp4_gb300 import MSAError, _lib, dequant_rows, synth
+from tests import _gpu, _wl
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.fixture(scope="module")
+def ragged():
+    # partial last pages, rows straddling a block boundary (130 tokens, 8 rows),
+    # a 1-token request, fewer than 16 blocks, up to 8 rows
+    return _wl.small([700, 130, 2000, 1, 4500, 3000], [3, 8, 1, 1, 5, 2], needles=2, seed=21)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_dequant_matches_oracle_for_every_scale_and_code(path):
+    scales = np.repeat(np.arange(0x80, dtype=np.uint8), 4)          # non-negative scales (NVFP4)
+    codes = np.tile(np.arange(256, dtype=np.uint8).reshape(4, 64), (0x80, 1))
+    sc = np.repeat(scales[:, None], 8, axis=1)
+    got = dequant_rows(torch.from_numpy(codes).cuda(), torch.from_numpy(np.ascontiguousarray(sc)).cuda(), path)
+    got = got.cpu().view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    tab = oracle.dequant_table()
+    c = np.stack([codes & 15, codes >> 4], axis=-1).reshape(-1, 128)
+    want = tab[scales[:, None].astype(np.int64), c.astype(np.int64)]
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_index_scores_match_oracle(ragged):
+    dec = _gpu.decoder(ragged)
+    s = dec.index_scores().cpu().numpy()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    for b in range(ragged.num_reqs):
+        N, R, r0 = _wl.geom(ragged, b)
+        ref = oracle.token_scores(ragged, b)                        # [R, 4, N]
+        got = s[r0:r0 + R, :, :N]
+        k = np.abs(_wl.keys_of(ragged, b, "ki"))
+        q = np.abs(_wl.e4m3_values()[ragged.q_idx[r0:r0 + R].astype(np.int64)])
+        bound = 8e-6 * np.einsum("rgd,td->rgt", q, k) + 1e-6
+        inf = np.isinf(ref)
+        assert np.array_equal(np.isinf(got), inf) and np.all(got[inf] < 0)
+        assert np.all(np.abs(got[~inf] - ref[~inf]) <= bound[~inf]), b
+
+
+def test_maxpool_topk_is_bitexact_on_given_scores(ragged):
+    big = _wl.small([9000, 40000, 130, 2047], [2, 8, 8, 1], needles=3, seed=5)
+    for wl in (ragged, big):
+        dec = _gpu.decoder(wl, with_block_scores=True)
+        stride = wl.max_pages_per_req * 128
+        S32 = np.full((wl.total_rows, 4, stride), np.nan, dtype=np.float32)
+        for b in range(wl.num_reqs):
+            N, R, r0 = _wl.geom(wl, b)
+            S32[r0:r0 + R, :, :N] = oracle.token_scores(wl, b).astype(np.float32)
+        ids = dec.maxpool_topk(torch.from_numpy(S32).cuda()).cpu().numpy()
+        bs = dec.block_scores.cpu().numpy()
+        torch.cuda.synchronize()
+        assert dec.errors() == 0
+        for b in range(wl.num_reqs):
+            N, R, r0 = _wl.geom(wl, b)
+            Sb = oracle.block_maxpool(S32[r0:r0 + R, :, :N].astype(np.float64))
+            nb = Sb.shape[1]
+            assert np.array_equal(bs[b, :, :nb], Sb.astype(np.float32))
+            assert np.all(np.isneginf(bs[b, :, nb:]))
+            for g in range(4):
+                assert np.array_equal(ids[b, g], oracle.select(Sb[g])), (b, g)
+
+
+def test_select_blocks_match_oracle(ragged):
+    wl = _wl.small([9000, 40000, 130, 2047, 700], [2, 8, 8, 1, 3], needles=3, seed=6)
+    dec = _gpu.decoder(wl, with_block_scores=True)
+    ids = dec.select_blocks().cpu().numpy()
+    bs = dec.block_scores.cpu().numpy()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    ref = oracle.decode(wl)
+    for i, b in enumerate(ref["reqs"]):
+        N = int(wl.context_lens[b])
+        nb = (N + 127) // 128
+        Sr = ref["S"][i][:, :nb]
+        np.testing.assert_allclose(bs[b, :, :nb], Sr, rtol=1e-5, atol=1e-4)
+        for g in range(4):
+            assert _gpu.selection_matches(ids[b, g], ref["ids"][i, g], Sr[g], nb), (b, g)
+
+
+def test_sparse_attention_on_oracle_ids(ragged):
+    r = oracle.decode(ragged)
+    dec = _gpu.decoder(ragged)
+    ids = torch.from_numpy(np.ascontiguousarray(r["ids"])).cuda()
+    out = dec.sparse_attn(ids).float().cpu().numpy()
+    lse = dec.lse.cpu().numpy()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    _gpu.assert_out_close(out, r["out"], "sparse attention")
+    np.testing.assert_allclose(lse, r["lse"], atol=1e-3, rtol=1e-4)
+
+
+@pytest.mark.parametrize("ctx,rows,needles,seed", [
+    ([4096], [1], 4, 0),                        # 32 blocks, one row
+    ([700, 130, 2000, 1, 4500, 3000], [3, 8, 1, 1, 5, 2], 2, 21),
+    ([20000], [8], 6, 8),                       # one request, 8 rows (64 query rows per group)
+    ([1500, 1500, 1500], [4, 4, 4], 0, 9),      # < 16 blocks: attend everything
+    ([66000, 33000], [1, 6], 5, 10),
+])
+def test_decode_matches_oracle(ctx, rows, needles, seed):
+    wl = _wl.small(ctx, rows, needles=needles, seed=seed)
+    _gpu.check_decode(wl)
+
+
+def test_decode_repeats_bitwise_with_one_workspace():
+    wl = _wl.small([30000, 5000, 70000], [8, 1, 4], needles=3, seed=12)
+    dec, _ = _gpu.check_decode(wl)
+    o1, i1 = dec.out.clone(), dec.block_ids.clone()
+    for _ in range(3):
+        dec.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(dec.block_ids, i1) and torch.equal(dec.out, o1)
+
+
+def test_permuted_block_table_gives_identical_results():
+    wl = _wl.small([30000, 5000], [8, 2], needles=3, seed=13)
+    d1 = _gpu.decoder(wl)
+    d1.decode()
+    d2 = _gpu.decoder(_wl.permuted_pages(wl))
+    d2.decode()
+    torch.cuda.synchronize()
+    assert torch.equal(d1.block_ids, d2.block_ids)
+    assert torch.equal(d1.out, d2.out)
+
+
+def test_shared_prefix_pages():
+    wl = _wl.small([2300, 4000, 2100, 9000], [2, 1, 4, 8], shared=16, seed=31)
+    _gpu.check_decode(wl)
+
+
+def test_empty_batch_and_zero_row_request():
+    wl = _wl.small([3000, 500], [0, 2], seed=3)
+    dec, _ = _gpu.check_decode(wl)
+    assert np.all(dec.block_ids[0].cpu().numpy() == -1)
+
+
+def test_host_rejects_bad_arguments_without_launching():
+    wl = _wl.small([3000], [1], seed=3)
+    dec = _gpu.decoder(wl)
+    a = _lib.make_args(dec.cache, dec.batch, wl.sm_scale)
+    a.head_dim = 64
+    with pytest.raises(MSAError) as e:
+        _lib.msa_decode(a, dec.block_ids, dec.out.view(torch.int16), None, dec.ws)
+    assert e.value.code == -2
+    a = _lib.make_args(dec.cache, dec.batch, wl.sm_scale)
+    with pytest.raises(MSAError) as e:
+        _lib.msa_decode(a, dec.block_ids, dec.out.view(torch.int16), None, dec.ws[:64])
+    assert e.value.code == -4
+    a.max_rows_per_req = 9
+    with pytest.raises(MSAError) as e:
+        _lib.msa_decode(a, dec.block_ids, dec.out.view(torch.int16), None, dec.ws)
+    assert e.value.code == -1
+
+
+@pytest.mark.parametrize("name", synth.PRESETS)
+def test_presets_full_size(name):
+    """The five workload shapes at full size, in the launch configuration the
+    benchmark times; the oracle checks every request (sampled for the largest)."""
+    wl = synth.make_workload(synth.preset(name))
+    reqs = None
+    if name == "ragged64":
+        reqs = list(range(0, 64, 4))
+    _, waived = _gpu.check_decode(wl, reqs)
+    assert waived <= 2
