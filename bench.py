@@ -1,0 +1,400 @@
+"""Benchmark of the MSA decode step (libmsa on GB300).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libmsa|reference] [--workload NAME]
+
+One step = one MSA decode pass (index scan -> block max pool -> top-16 ->
+sparse attention) over a batch of synthetic inputs already resident in HBM;
+the default workload is 16 requests x 131,072-token context x 8 speculative
+query rows. Prints one JSON line (rank 0). Under torchrun with N>1 every rank
+runs an independent replica on its own GPU (the decode of independent requests
+needs no exchange); value = all ranks' query rows / the slowest rank's time.
+
+--impl reference times the oracle (plain FP64 CPU restatement of the method) on
+the host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA decode query-rows/s at 128K ctx; achieved HBM GB/s vs ~8 TB/s roofline"
+UNIT = "query-rows/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, or None.
+    The summary names the kernel source hash it was taken on; a different hash
+    (the kernel changed since) gives None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_sparse_attention_nvfp4_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons of one GPU during a region
+    (NVML through ctypes every few ms; nvidia-smi as a fallback). Read-only."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, uuid: str, period_s: float = 0.002):
+        self.uuid, self.period = uuid, period_s
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._h = None
+        self._proc = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    m = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                        self.max_mhz = int(m.value)
+        except OSError:
+            pass
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(int(mhz.value))
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", self.uuid, "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE, text=True)
+            except OSError:
+                self._proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+        elif self._proc is not None:
+            self._proc.terminate()
+            out = self._proc.communicate()[0]
+            for line in out.splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 3 and parts[0].isdigit():
+                    self.samples.append(int(parts[0]))
+                    self.max_mhz = int(parts[1])
+                    self.reasons |= int(parts[2], 16)
+
+    def summary(self):
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+def reduce_over_ranks(local_seconds: float, local_units: float, dist=None):
+    """Whole-job numbers: units summed over ranks, time = the slowest rank's."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return local_seconds, local_units
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def workload_config(name, spec, l2_note):
+    rows = list(spec.rows)
+    ctx = list(spec.context_lens)
+    return {"workload": name,
+            "description": f"{len(ctx)} requests, context {min(ctx)}..{max(ctx)} tokens, {min(rows)}..{max(rows)} "
+                           "query rows per request (speculative rows causal among themselves); 4 KV heads x d=128, "
+                           "8 FP8 query heads per KV head, 1 shared index-key head; NVFP4 K/V/index caches "
+                           "(E2M1 + E4M3 scale per 16) in 128-token pages behind a shuffled block table; top-16 "
+                           "blocks per group with the recent block kept",
+            "requests": len(ctx), "context_tokens": max(ctx) if len(set(ctx)) == 1 else "mixed",
+            "rows_per_request": rows[0] if len(set(rows)) == 1 else "mixed", "query_rows_per_step": int(sum(rows)),
+            "needles_per_group": spec.needles_per_group, "seed": spec.seed, "l2": l2_note}
+
+
+# ----------------------------------------------------------------------------- libmsa arm
+def run_libmsa(args, rank, world, dist):
+    import torch
+
+    import oracle
+    from block_sparse_attention_nvfp4_gb300 import DecodeBatch, KVCache, MSADecoder
+    from block_sparse_attention_nvfp4_gb300 import bytes_model as bm
+    from block_sparse_attention_nvfp4_gb300 import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    spec = synth.preset(args.workload)
+    wl = synth.make_workload(spec)
+    cache, batch = KVCache.from_host(wl), DecodeBatch.from_host(wl)
+    dec = MSADecoder(cache, batch, sm_scale=wl.sm_scale, with_lse=True)
+    rows = int(wl.total_rows)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def l2_flush():
+        flush.zero_()
+
+    for _ in range(args.warmup):
+        l2_flush()
+        dec.decode()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0, "device error flags after warm-up"
+
+    # ---- timed region: K decode steps, L2 flushed before each (flush outside the events)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    uuid = str(torch.cuda.get_device_properties(local).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    sampler = ClockSampler(uuid)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            l2_flush()
+            ev[i][0].record(stream)
+            dec.decode()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dev_seconds = sum(step_ms) / 1e3
+    t_max, units = reduce_over_ranks(dev_seconds, float(rows * args.steps), dist)
+    value = units / t_max
+    ms_per_step = statistics.mean(step_ms)
+    ok_flags = dec.errors()
+
+    # ---- dominant kernel alone (selection: index scan + max pool + top-k), same flushing
+    kr = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
+    for i in range(kr):
+        l2_flush()
+        evs[i][0].record(stream)
+        dec.select_blocks()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    sel_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ids_now = dec.block_ids.clone()
+    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
+    for i in range(kr):
+        l2_flush()
+        eva[i][0].record(stream)
+        dec.sparse_attn(ids_now)
+        eva[i][1].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in eva)
+
+    sel_bytes = bm.select_bytes(wl.context_lens, np.diff(wl.q_indptr))
+    step_bytes = bm.step_bytes(wl.context_lens, np.diff(wl.q_indptr), ids_now.cpu().numpy())
+    peak, peak_kind = measured_peaks()
+    achieved = sel_bytes / (sel_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "select_kernel (index scan + block max pool + top-k)",
+                "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profile_traffic("select_kernel", args.workload),
+                "algorithmic_bytes_per_launch": sel_bytes, "avg_launch_us": round(sel_ms * 1e3, 2)}
+
+    # ---- end to end through the public API: host buffers, copies inside the timed region
+    ke = min(args.steps, 50)
+    h_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
+            for k in ("context_lens", "q_indptr", "block_table", "q", "q_idx")}
+    h_out = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    h_ids = torch.empty(dec.block_ids.shape, dtype=dec.block_ids.dtype).pin_memory()
+    h_lse = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_ids, h_lse))
+    torch.cuda.synchronize()
+    e2e_times = []
+    for i in range(ke + 2):
+        l2_flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k, t in h_in.items():
+            getattr(batch, k).copy_(t, non_blocking=True)
+        dec.decode()
+        h_out.copy_(dec.out, non_blocking=True)
+        h_ids.copy_(dec.block_ids, non_blocking=True)
+        h_lse.copy_(dec.lse, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 2:
+            e2e_times.append(time.perf_counter() - t0)
+    e2e_t, e2e_u = reduce_over_ranks(sum(e2e_times), float(rows * ke), dist)
+    e2e = {"value": round(e2e_u / e2e_t, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "steps": ke,
+           "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4)}
+
+    # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        reqs = list(range(min(wl.num_reqs, 16)))
+        t0 = time.perf_counter()
+        oracle.decode(wl, reqs)
+        dt = time.perf_counter() - t0
+        srows = int(sum(int(wl.q_indptr[b + 1] - wl.q_indptr[b]) for b in reqs))
+        cpu = {"value": round(srows / dt, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{len(reqs)} of {wl.num_reqs} requests of the same workload ({srows} query rows), "
+                         f"one pass, {dt:.2f} s wall"}
+
+    clocks = sampler.summary()
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": dict(workload_config(args.workload, spec, "flushed before every timed step (512 MiB write)"),
+                           parallelism=f"replicas x{world}"),
+            "hbm_gbs_step": round(step_bytes["total"] / (ms_per_step * 1e-3) / 1e9, 1),
+            "step_bytes": step_bytes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "kernels_us": {"decode": round(ms_per_step * 1e3, 2), "select": round(sel_ms * 1e3, 2),
+                           "sparse_attention": round(attn_ms * 1e3, 2)},
+            "clocks": clocks, "timed_wall_s": round(wall, 4), "device_error_flags": ok_flags,
+            "impl": "libmsa"}
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm (oracle)
+def run_reference(args):
+    import oracle
+    from block_sparse_attention_nvfp4_gb300 import synth
+
+    spec = synth.preset(args.workload)
+    wl = synth.make_workload(spec)
+    oracle.build()
+    # per step: one request of the workload through the whole oracle path; if K+W
+    # such steps would exceed the time budget, a step takes one query row's share
+    t0 = time.perf_counter()
+    oracle.decode(wl, [0])
+    one = time.perf_counter() - t0
+    budget = 240.0
+    reqs_per_step = 1
+    rows_per_req = int(wl.q_indptr[1] - wl.q_indptr[0])
+    steps_total = args.steps + args.warmup
+    note = "one request per step (all its query rows), full path"
+    for i in range(args.warmup):
+        oracle.decode(wl, [i % wl.num_reqs])
+    times = []
+    projected = steps_total * one
+    if projected > budget:
+        # bounded: time one request per (budget / one) steps and spread it evenly
+        per = max(1, int(math.ceil(projected / budget)))
+        note = f"one request every {per} steps (time spread over those steps): budget {budget:.0f} s"
+    else:
+        per = 1
+    total = 0.0
+    units = 0.0
+    for i in range(args.steps):
+        if i % per == 0:
+            t0 = time.perf_counter()
+            oracle.decode(wl, [i % wl.num_reqs])
+            total += time.perf_counter() - t0
+            units += rows_per_req * reqs_per_step
+    value = units / total
+    return {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * total / max(1, args.steps // per), 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(workload_config(args.workload, spec, "n/a (host)"), parallelism="host cores"),
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": note},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="libmsa", choices=["libmsa", "reference"])
+    ap.add_argument("--workload", default="spec8_128k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        tdist.init_process_group("nccl")
+        dist = tdist
+    if world == 1 and args.gpus != 1:
+        raise SystemExit("--gpus N>1 runs under torchrun (one process per GPU)")
+    import __graft_entry__
+    __graft_entry__.build()
+    line = run_libmsa(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

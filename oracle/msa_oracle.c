@@ -159,23 +159,29 @@ static int page_of(const oracle_args* a, int b, int block) {
 int oracle_token_scores(const oracle_args* a, int b, double* s) {
   int N, R, row0, t, r, g, j, rc;
   double kv[OR_D];
+  double* qd;
   oracle_dequant_table(NULL);
   if ((rc = req_geometry(a, b, &N, &R, &row0)) != OR_OK) return rc;
+  /* the request's index queries as values, [r][g][j] */
+  qd = (double*)malloc(sizeof(double) * ((size_t)R * OR_G * OR_D + 1));
+  if (!qd) return OR_ENOMEM;
+  for (j = 0; j < R * OR_G * OR_D; j++) qd[j] = oracle_e4m3_value(a->q_idx[(int64_t)row0 * OR_G * OR_D + j]);
   for (t = 0; t < N; t++) {
     int page = page_of(a, b, t / OR_BLK), slot = t % OR_BLK;
-    if (page < 0) return OR_EINVAL;
+    if (page < 0) { free(qd); return OR_EINVAL; }
     dequant_row(a->ki_data + ((int64_t)page * OR_BLK + slot) * 64, a->ki_scale + ((int64_t)page * OR_BLK + slot) * 8, kv);
     for (r = 0; r < R; r++) {
       int pos = N - R + r;
       for (g = 0; g < OR_G; g++) {
         double acc = 0.0;
-        const uint8_t* qi = a->q_idx + ((int64_t)(row0 + r) * OR_G + g) * OR_D;
+        const double* qi = qd + ((size_t)r * OR_G + g) * OR_D;
         if (t > pos) { s[((int64_t)r * OR_G + g) * N + t] = -INFINITY; continue; }
-        for (j = 0; j < OR_D; j++) acc += oracle_e4m3_value(qi[j]) * kv[j];
+        for (j = 0; j < OR_D; j++) acc += qi[j] * kv[j];
         s[((int64_t)r * OR_G + g) * N + t] = acc;
       }
     }
   }
+  free(qd);
   return OR_OK;
 }
 
@@ -294,13 +300,14 @@ int oracle_attend(const oracle_args* a, int b, const int32_t* ids, double* out, 
       int pos = N - R + r;
       for (hh = 0; hh < OR_HQ / OR_G; hh++) {
         int h = g * (OR_HQ / OR_G) + hh;
-        const uint8_t* qv = a->q + ((int64_t)(row0 + r) * OR_HQ + h) * OR_D;
-        double m = -INFINITY, l = 0.0, o[OR_D];
+        const uint8_t* qb = a->q + ((int64_t)(row0 + r) * OR_HQ + h) * OR_D;
+        double m = -INFINITY, l = 0.0, o[OR_D], qv[OR_D];
         int any = 0;
+        for (j = 0; j < OR_D; j++) qv[j] = oracle_e4m3_value(qb[j]);
         for (i = 0; i < nkeys; i++) {
           double acc = 0.0;
           if (kpos[i] > pos) { logit[i] = -INFINITY; continue; }
-          for (j = 0; j < OR_D; j++) acc += oracle_e4m3_value(qv[j]) * kd[(size_t)i * OR_D + j];
+          for (j = 0; j < OR_D; j++) acc += qv[j] * kd[(size_t)i * OR_D + j];
           logit[i] = acc * a->sm_scale;
           if (logit[i] > m) m = logit[i];
           any = 1;
