@@ -24,8 +24,8 @@ FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS = 0x1, 0x2, 0x4, 0x8
 
 # symbols include/msa.h declares (checked by the CPU tests)
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
-           "msa_block_maxpool_topk", "msa_select_blocks", "msa_sparse_attn_decode", "msa_decode",
-           "msa_dequant_rows")
+           "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
+           "msa_decode", "msa_dequant_rows")
 
 
 class MSAError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
             lib.msa_index_scores.argtypes = [ap, vp, i64, vp, sz, vp]
             lib.msa_block_maxpool_topk.argtypes = [ap, vp, i64, vp, vp, vp, sz, vp]
             lib.msa_select_blocks.argtypes = [ap, vp, vp, vp, sz, vp]
+            lib.msa_select_blocks_noalloc.argtypes = [ap, vp, vp, vp]
             lib.msa_sparse_attn_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_dequant_rows.argtypes = [vp, vp, i64, vp, ctypes.c_int32, vp]
@@ -153,6 +154,14 @@ def msa_select_blocks(args: Args, block_ids: torch.Tensor, block_scores: Optiona
                       stream=None):
     _check(load().msa_select_blocks(ctypes.byref(args), _ptr(block_ids), _ptr(block_scores), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "msa_select_blocks")
+
+
+def msa_select_blocks_noalloc(args: Args, block_ids: torch.Tensor, block_scores: Optional[torch.Tensor],
+                              stream=None):
+    """msa_select_blocks without a caller workspace (scratch inside the library;
+    see include/msa.h for the size limit and the sharing rules)."""
+    _check(load().msa_select_blocks_noalloc(ctypes.byref(args), _ptr(block_ids), _ptr(block_scores),
+                                            _stream(stream)), "msa_select_blocks_noalloc")
 
 
 def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],

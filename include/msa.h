@@ -158,6 +158,24 @@ msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, fl
 msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* block_ids,
                                   uint16_t* out_bf16, float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/* msa_select_blocks for callers that cannot allocate device memory. The MSA
+ * pages have no counterpart to this entry point; it exists for hosts that hand a
+ * library only the tensors it works on and keep the allocator to themselves
+ * (plugin / custom-operator interfaces), and for decode loops that must not call
+ * cudaMalloc because it can synchronise the device. It runs the same kernel as
+ * msa_select_blocks with the same outputs, but its scratch (error flags, arrival
+ * counters, partial block maxima: 256 + 4*B + 64*B*max_pages_per_req bytes, rounded
+ * up to 256) lives in a fixed 8 MiB device buffer inside the library, which every
+ * GPU that loads libmsa holds until the process exits. Batches needing more return
+ * MSA_ERR_WORKSPACE before any launch. It allocates nothing: the first call on each
+ * device looks the buffer's address up once (make that first call before any
+ * stream capture), and every call clears the flags and counters with an async
+ * memset on `stream`. All calls share the one buffer, so calls that overlap on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller. Device error flags are cleared per call and not reported. */
+msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
+                                     void* stream);
+
 /* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, the
  * second launch chained to the first with programmatic dependent launch. */
 msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse,
