@@ -153,6 +153,7 @@ SelectParams select_params(const msa_decode_args* a, const Ws& w, int32_t* ids, 
   p.q_idx = a->q_idx;
   p.ki_scale = a->ki_scale;
   p.block_S = w.block_S;
+  p.s_stride = score_stride(a->max_pages_per_req);
   p.req_cnt = w.req_cnt;
   p.flags = w.flags;
   p.block_ids = ids;
@@ -191,9 +192,10 @@ AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, 
 
 }  // namespace
 
+int score_stride(int max_pages) { return (max_pages + 3) / 4 * 4; }
+
 Plan make_plan(int num_reqs, int sm_count) {
   Plan pl;
-  pl.select_grid = 2 * sm_count;  // two resident CTAs per SM (tensor memory: 256 columns each)
   const int pairs = num_reqs * kGroups;
   const int target = 2 * sm_count;
   int bps = pairs > 0 ? pow2_floor((kTopK * pairs) / target) : kTopK;
@@ -215,7 +217,7 @@ WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_p
   L.pair_cnt = off;
   off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs) * kGroups);
   L.block_S = off;
-  off = align_up(off + sizeof(float) * 4 * static_cast<size_t>(num_reqs) * kGroups * max_pages);
+  off = align_up(off + sizeof(float) * static_cast<size_t>(num_reqs) * kGroups * score_stride(max_pages));
   const size_t m = static_cast<size_t>(kQPerKV) * max_rows_per_req;
   const size_t parts = plan.splits > 1 ? static_cast<size_t>(plan.splits) * num_reqs * kGroups * m : 0;
   L.part_o = off;
@@ -288,7 +290,7 @@ static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids
   SelectParams p = select_params(args, w, ids, scores_out);
   p.token_scores = tok;
   p.score_stride = stride;
-  return launch_select(map, p, mode, plan.select_grid, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return launch_select(map, p, mode, d.sm_count, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 msa_status msa_index_scores(const msa_decode_args* args, float* scores, int64_t score_stride, void* ws,
@@ -330,6 +332,7 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
   p.scores = scores;
   p.score_stride = score_stride;
   p.block_S = w.block_S;
+  p.s_stride = msa::score_stride(args->max_pages_per_req);
   p.block_ids = block_ids;
   p.block_scores_out = block_scores;
   p.flags = w.flags;

@@ -272,47 +272,76 @@ __device__ __forceinline__ void dq8_split(uint32_t w, const LutEntry& L, uint32_
 // [vLLM-zh §How; MSA-fig §1 TopK] One warp selects the blocks of one group:
 // the most recent block (nb-1) plus the 15 best of blocks 0..nb-2 by score,
 // ties to the lower id; every block when nb <= 16. ids_out gets 16 ascending
-// ids, -1 padded. S is read with plain loads (written by this or other CTAs
-// before a device-scope fence). fmaxf ignores a NaN partial; a block whose
-// partials are all NaN ranks last.
+// ids, -1 padded. S[c] is block c's score (written by this or other CTAs before
+// a device-scope fence; read with plain loads, 16-byte aligned rows).
+//
+// Ranking key: the score's order-preserving integer image in the high word and
+// the complemented block id in the low word, so larger key = higher score, then
+// lower id; NaN ranks below everything.
 __device__ __forceinline__ uint64_t topk_key(float v, int id) {
   uint32_t u = __float_as_uint(v);
   uint32_t hi;
-  if (v != v) hi = 0u;                       // NaN ranks below everything
+  if (v != v) hi = 0u;
   else hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return (static_cast<uint64_t>(hi) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(id));
 }
+__device__ __forceinline__ int topk_id(uint64_t key) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
+  const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+// Value of candidate slot c (c < nc) as a key; 0 (below every real key) past the end.
+__device__ __forceinline__ uint64_t cand_key(const float* S, int c, int nc) {
+  return c < nc ? topk_key(S[c], c) : 0ull;
+}
 
-__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
-
-// S[c] holds partial maxima of block c (their max is the block score).
-static __device__ __noinline__ void warp_topk(const float4* S, int nb, int32_t* ids_out) {
+// Warp-wide descending bitonic sort of one u64 per lane.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
   const int lane = threadIdx.x & 31;
-  if (nb <= kTopK) {
-    if (lane < kTopK) ids_out[lane] = lane < nb ? lane : -1;
-    return;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = shfl_xor_u64(v, j);
+      const bool up = (lane & k) == 0;          // this k-block sorts descending
+      const bool lower = (lane & j) == 0;       // this lane keeps the larger when descending
+      const bool keep_max = (up == lower);
+      v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+    }
   }
+  return v;
+}
+
+// Exact top-(kTopK-1) of nc candidates by insertion into per-lane sorted lists
+// and a 15-round warp merge; the fallback when the threshold filter keeps too many.
+static __device__ __noinline__ void topk_by_insertion(const float* S, int nc, int32_t* sel) {
+  const int lane = threadIdx.x & 31;
   constexpr int L = kTopK - 1;
   uint64_t list[L];
 #pragma unroll
   for (int j = 0; j < L; ++j) list[j] = 0ull;
-  for (int c = lane; c < nb - 1; c += 32) {
-    const uint64_t key = topk_key(max4(S[c]), c);
+  for (int c = lane; c < nc; c += 32) {
+    const uint64_t key = topk_key(S[c], c);
     if (key > list[L - 1]) {
 #pragma unroll
       for (int j = L - 1; j > 0; --j) list[j] = (key > list[j - 1]) ? list[j - 1] : ((key > list[j]) ? key : list[j]);
       list[0] = key > list[0] ? key : list[0];
     }
   }
-  int my_id = nb - 1;  // lane 15 keeps the recent block
 #pragma unroll 1
   for (int k = 0; k < L; ++k) {
     uint64_t best = list[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(best), off);
-      const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(best >> 32), off);
-      const uint64_t o = (static_cast<uint64_t>(hi) << 32) | lo;
+      const uint64_t o = shfl_xor_u64(best, off);
       best = o > best ? o : best;
     }
     if (list[0] == best) {  // keys are unique per block id: exactly one lane
@@ -320,15 +349,84 @@ static __device__ __noinline__ void warp_topk(const float4* S, int nb, int32_t* 
       for (int j = 0; j < L - 1; ++j) list[j] = list[j + 1];
       list[L - 1] = 0ull;
     }
-    if (lane == k) my_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
+    if (lane == 0) sel[k] = topk_id(best);
   }
-  // ascending order: rank among lanes 0..15
+  __syncwarp();
+}
+
+// scratch: 64 u64 per warp (shared memory), for the threshold filter's survivors.
+static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* ids_out, uint64_t* scratch) {
+  const int lane = threadIdx.x & 31;
+  if (nb <= kTopK) {
+    if (lane < kTopK) ids_out[lane] = lane < nb ? lane : -1;
+    return;
+  }
+  constexpr int L = kTopK - 1;
+  const int nc = nb - 1;  // candidates: every block but the recent one
+  int32_t* sel = reinterpret_cast<int32_t*>(scratch + 48);  // 15 winners (kept apart from survivors 0..47)
+  // 1. each lane's best key; loads issued 8 at a time (4 blocks per 16-byte load)
+  uint64_t lmax = 0ull;
+  for (int base = 0; base < nc; base += 32 * 4 * 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = base + (u * 32 + lane) * 4;
+      v[u] = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = base + (u * 32 + lane) * 4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (c + q < nc) {
+          const uint64_t k = topk_key(e[q], c + q);
+          lmax = k > lmax ? k : lmax;
+        }
+    }
+  }
+  // 2. the 15th largest lane maximum bounds the answer: the 15 largest lane maxima
+  //    are 15 distinct candidates, so the 15th best candidate is at least that large
+  const uint64_t T = shfl_u64(warp_sort_desc(lmax), L - 1);
+  // 3. survivors: every candidate with key >= T (contains the exact top 15)
+  int count = 0;
+  for (int base = 0; base < nc; base += 32 * 4) {
+    const int c = base + lane * 4;
+    float4 v = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool keep = c + q < nc && topk_key(e[q], c + q) >= T;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+      if (keep) {
+        const int pos = count + __popc(bal & ((1u << lane) - 1u));
+        if (pos < 48) scratch[pos] = topk_key(e[q], c + q);
+      }
+      count += __popc(bal);
+    }
+  }
+  __syncwarp();
+  if (count > 48) {
+    topk_by_insertion(S, nc, sel);
+  } else {
+    // 4. exact rank among the survivors
+    for (int i = lane; i < count; i += 32) {
+      const uint64_t k = scratch[i];
+      int rank = 0;
+      for (int j = 0; j < count; ++j) rank += scratch[j] > k ? 1 : 0;
+      if (rank < L) sel[rank] = topk_id(k);
+    }
+    __syncwarp();
+  }
+  // 5. the 15 winners plus the recent block, ascending
+  int my_id = lane < L ? sel[lane] : nb - 1;
   int rank = 0;
 #pragma unroll
   for (int j = 0; j < kTopK; ++j) {
     const int other = __shfl_sync(0xFFFFFFFFu, my_id, j);
     rank += (other < my_id) ? 1 : 0;
   }
+  __syncwarp();
   if (lane < kTopK) ids_out[rank] = my_id;
 }
 

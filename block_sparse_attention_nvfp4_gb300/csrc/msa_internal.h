@@ -16,7 +16,8 @@ struct SelectParams {
   const int32_t* block_table;
   const uint8_t* q_idx;
   const uint8_t* ki_scale;
-  float* block_S;           // workspace [B][4][max_pages][4 partials]
+  float* block_S;           // workspace [B][4][s_stride] block scores
+  int s_stride;             // max_pages rounded up to a multiple of 4 (16-byte rows)
   uint32_t* req_cnt;        // workspace [B] arrival counters
   uint32_t* flags;          // workspace error flags
   int32_t* block_ids;       // [B][4][16]
@@ -32,6 +33,7 @@ struct MaxpoolParams {
   const float* scores;
   long long score_stride;
   float* block_S;
+  int s_stride;
   int32_t* block_ids;
   float* block_scores_out;
   uint32_t* flags;
@@ -67,17 +69,19 @@ struct WsLayout {
 };
 
 struct Plan {
-  int select_grid;        // CTAs of the scan kernel
   int blocks_per_split;   // attention
   int splits;
 };
 
 Plan make_plan(int num_reqs, int sm_count);
+int score_stride(int max_pages);  // block-score row length: max_pages rounded up to 4
 WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan);
 
 size_t select_smem_bytes(int num_reqs);
 size_t attn_smem_bytes();
-cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int grid, cudaStream_t st);
+// grid: a fixed number of CTAs per SM over `sm_count` SMs
+cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,
+                          cudaStream_t st);
 cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
 cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,

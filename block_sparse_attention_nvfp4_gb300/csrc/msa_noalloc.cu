@@ -7,8 +7,8 @@
 // must not call cudaMalloc at all, because it can synchronise the device and
 // stall every other stream. Such callers cannot provide the workspace that
 // msa_select_blocks takes. This entry point runs the same kernel with its
-// scratch (device error flags, per-request arrival counters, per-block partial
-// maxima) in a fixed buffer compiled into the library instead.
+// scratch (device error flags, per-request arrival counters, block scores) in
+// a fixed buffer compiled into the library instead.
 //
 // The buffer is kScratchBytes (8 MiB) of device memory that every GPU which
 // loads libmsa holds until the process exits. All calls share it, so calls that
@@ -79,11 +79,11 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
       (reinterpret_cast<uintptr_t>(args->ki_scale) & 15u))
     return MSA_ERR_INVALID_ARG;
 
-  // scratch layout: error flags | arrival counters [B] | partial block maxima [B][4][max_pages][4]
+  // scratch layout: error flags | arrival counters [B] | block scores [B][4][max_pages rounded up to 4]
   const size_t off_cnt = 256;
   const size_t off_S = align256(off_cnt + sizeof(uint32_t) * static_cast<size_t>(args->num_reqs));
   const size_t need =
-      off_S + sizeof(float) * 4 * static_cast<size_t>(args->num_reqs) * kGroups * args->max_pages_per_req;
+      off_S + sizeof(float) * static_cast<size_t>(args->num_reqs) * kGroups * score_stride(args->max_pages_per_req);
   if (need > kScratchBytes) return MSA_ERR_WORKSPACE;  // the batch needs more than the fixed buffer holds
 
   int dev = 0, maj = 0, mi = 0, sms = 0;
@@ -135,7 +135,8 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
   p.flags = reinterpret_cast<uint32_t*>(s);
   p.req_cnt = reinterpret_cast<uint32_t*>(s + off_cnt);
   p.block_S = reinterpret_cast<float*>(s + off_S);
+  p.s_stride = score_stride(args->max_pages_per_req);
   p.block_ids = block_ids;
   p.block_scores_out = block_scores;
-  return launch_select(map, p, 0, 2 * sms, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return launch_select(map, p, 0, sms, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

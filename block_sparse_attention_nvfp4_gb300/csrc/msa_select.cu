@@ -10,26 +10,31 @@
 // FP8 MMA [vLLM-zh, Blackwell kernels].
 //
 // Design (GB300, sm_103a). Decode reads the whole index-key cache every step, so
-// this kernel is a stream over the cache's pages at HBM speed:
-//   * One CTA = 4 "row" warps (thread = token of the current page = TMEM lane)
-//     + 1 "issue" warp. A grid of 2 CTAs per SM takes equal contiguous ranges
-//     of all requests' pages.
-//   * The issue warp's elected lane streams pages into a ring of shared-memory
-//     stages with TMA (codes: 2-D tensor copy with 64-byte swizzle, so each row
-//     thread reads its 64-byte row without bank conflicts; scales: 1-D bulk copy)
-//     and issues the tensor-core MMAs.
-//   * Row threads dequantise their token's 128 elements into positive/negative
-//     magnitude parts (byte-permute table lookups) and store them into tensor
-//     memory as the A operand; the MMA computes scores = A x q_idx^T for all
-//     4 x R index-query columns of the request (B = q_idx in shared memory),
-//     accumulating in FP32 in tensor memory, the negative part through the
-//     negate-B bit. Products of two E4M3 values are exact; only the FP32 sums
-//     round.
-//   * The epilogue reads each token's scores from tensor memory, applies the
-//     causal mask, takes the max over the group's rows and over the block's
-//     128 tokens and writes one FP32 block score per (request, group, block).
-//   * The CTA that completes a request's block scores (an arrival counter, no
-//     waiting) runs the top-k for that request: one warp per group.
+// this kernel is a stream over the cache's pages at HBM speed. One CTA has three
+// roles, 2 CTAs per SM (256 TMEM columns each), the grid taking equal contiguous
+// ranges of all requests' pages:
+//   * load warp: one lane streams pages into a ring of shared-memory stages with
+//     TMA (codes: 2-D tensor copy with 64-byte swizzle, so each thread reads its
+//     64-byte row without bank conflicts; scales: 1-D bulk copy);
+//   * MMA warp: one lane issues the tensor-core MMAs (a single issuing thread
+//     sustains about one MMA per 45 cycles, so it does nothing else); the warp
+//     rewrites the index-query tile (B operand) when the request changes;
+//   * 4 dequant warps (thread = token of the page = TMEM lane): dequantise their
+//     token's 128 elements into positive/negative magnitude parts (byte-permute
+//     table lookups) and store them into a 3-deep ring of tensor-memory A
+//     buffers; the MMA computes scores = A x q_idx^T for the 4 x R index-query
+//     columns of the request, FP32 accumulation in tensor memory, the negative
+//     part through the negate-B bit (products of two E4M3 values are exact; only
+//     the FP32 sums round);
+//   * 4 epilogue warps: read each page's scores from a 2-deep ring of tensor-
+//     memory D buffers, mask, max-pool over the group's rows and their 32 tokens
+//     and write one partial per warp and block.
+// The dequant warps never wait for an MMA result, only for a free A buffer, so
+// the MMA round trip hides behind the next pages' dequantisation. The CTA that
+// completes a request's block scores (an arrival counter, no waiting) runs the
+// top-k for that request: one warp per group.
+#include <climits>
+
 #include "msa_common.cuh"
 #include "msa_internal.h"
 
@@ -37,15 +42,20 @@ namespace msa {
 
 namespace {
 
-constexpr int kRowWarps = 4;
-constexpr int kThreads = (kRowWarps + 1) * 32;
+constexpr int kRowWarps = 4;                       // dequant warps = epilogue warps
+constexpr int kThreads = (2 * kRowWarps + 2) * 32;  // + the MMA warp + the TMA warp
+constexpr int kIssueWarp = 2 * kRowWarps;          // MMA issue, query tile
+constexpr int kLoadWarp = 2 * kRowWarps + 1;       // TMA producer
+constexpr int kCtasPerSm = 2;
 constexpr int kStages = 6;
+constexpr int kABufs = 3, kDBufs = 2;
 constexpr uint32_t kCodeBytes = kBlock * 64;    // one page of index-key codes
 constexpr uint32_t kScaleBytes = kBlock * 8;    // its scales
 constexpr uint32_t kTmemCols = 256;
-// TMEM columns: A buffers (positive part 32 cols + negative part 32 cols) x2,
-// then D (scores, up to 32 FP32 columns) x2.
-constexpr uint32_t kColA0 = 0, kColD0 = 128;
+constexpr int kCtaPages = 2048;                  // block-table entries staged per CTA
+// TMEM columns: kABufs A buffers (positive part 32 cols + negative part 32 cols),
+// then kDBufs D buffers (scores, up to 32 FP32 columns).
+constexpr uint32_t kColA = 0, kColD = 64 * kABufs;
 
 struct Smem {
   LutEntry lut[256];                        // 4 KB
@@ -53,8 +63,11 @@ struct Smem {
   uint8_t qtile[32 * 128];                  // B operand: up to 32 index-query rows x 128 (SW128)
   uint8_t scales[kStages][kScaleBytes];
   uint64_t full[kStages], empty[kStages];
-  uint64_t afull[2], dfull[2], dempty[2];
+  uint64_t afull[kABufs], afree[kABufs], dfull[kDBufs], dempty[kDBufs];
   int stage_bad[kStages];
+  int slot_max[4][kGroups];                 // per-page ring: ordered-int max of the epilogue warps' partials
+  int slot_cnt[4];                          // epilogue warps that have contributed to the slot
+  int32_t phys[kCtaPages];                  // this CTA's block-table entries (when its range fits)
   uint32_t taddr;
   int ntodo;
 };
@@ -86,12 +99,77 @@ __device__ __forceinline__ PageCursor cursor_at(long long p, const long long* pr
   return pc;
 }
 
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t* flags) {
+  return mbar_try(bar, parity) || mbar_wait(bar, parity, flags);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+// order-preserving int image of a float (for atomicMax), and back
+__device__ __forceinline__ int ord_of(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float float_of(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7FFFFFFF)); }
+
+__device__ __forceinline__ uint32_t bitnot_fma(uint32_t w) {  // ~w on the multiply-add pipe
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %2;" : "=r"(r) : "r"(w), "r"(0xFFFFFFFFu));
+  return r;
+}
+
+// Group maxima of a fully visible token: columns n = rq*4 + g, rq < R.
+template <int R>
+__device__ __forceinline__ void group_max(const uint32_t (&dv)[32], float (&mg)[kGroups]) {
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    float m = __uint_as_float(dv[g]);
+#pragma unroll
+    for (int rq = 1; rq < R; rq += 2) {
+      const float a = __uint_as_float(dv[rq * kGroups + g]);
+      const float b = rq + 1 < R ? __uint_as_float(dv[(rq + 1) * kGroups + g]) : a;
+      m = fmax3(m, a, b);
+    }
+    mg[g] = m;
+  }
+}
+
+// Dequantise 8 code words (4 groups of scale bytes sb0..sb3 = words 2k, 2k+1)
+// into 16 positive-part and 16 negative-part words and store them to TMEM.
+__device__ __forceinline__ void dequant_store_half(const LutEntry* lut, const uint32_t* w, uint32_t scw,
+                                                   uint32_t a_pos, uint32_t a_neg) {
+  uint32_t pa[16], na[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const LutEntry L = lut[(scw >> (8 * q)) & 0xFFu];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t x = w[2 * q + h];
+      const uint32_t xh = x >> 16;
+      pa[4 * q + 2 * h] = prmt(L.p0, L.p1, x);
+      pa[4 * q + 2 * h + 1] = prmt(L.p0, L.p1, xh);
+      na[4 * q + 2 * h] = prmt(L.n0, L.n1, bitnot_fma(x));
+      na[4 * q + 2 * h + 1] = prmt(L.n0, L.n1, bitnot_fma(xh));
+    }
+  }
+  tmem_st16(a_pos, pa);
+  tmem_st16(a_neg, na);
+}
+
 }  // namespace
 
 // MODE 0: fused select (block scores + top-k). MODE 1: write per-token scores
 // (msa_index_scores) and stop.
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     select_kernel(const __grid_constant__ CUtensorMap ki_map, const SelectParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem_al = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // TMA/UMMA tiles need 1 KB
@@ -164,29 +242,59 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kRowWarps);
     }
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kABufs; ++j) {
       mbar_init(smem_u32(&sm.afull[j]), kRowWarps);
-      mbar_init(smem_u32(&sm.dfull[j]), 1);
-      mbar_init(smem_u32(&sm.dempty[j]), kRowWarps);
+      mbar_init(smem_u32(&sm.afree[j]), 1);
+    }
+    for (int k = 0; k < kDBufs; ++k) {
+      mbar_init(smem_u32(&sm.dfull[k]), 1);
+      mbar_init(smem_u32(&sm.dempty[k]), kRowWarps);
     }
     mbar_fence_init();
   }
-  if (warp == kRowWarps) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
+  if (tid < 4 * kGroups) sm.slot_max[tid / kGroups][tid % kGroups] = INT_MIN;
+  if (tid < 4) sm.slot_cnt[tid] = 0;
+  // this CTA's block-table entries, so no page waits on a dependent global load
+  const bool staged = n <= kCtaPages;
+  if (staged) {
+    for (int i = tid; i < n; i += kThreads) {
+      const PageCursor pc = cursor_at(p0 + i, prefix, B);
+      sm.phys[i] = p.block_table[static_cast<long long>(pc.b) * p.max_pages + pc.c];
+    }
+  }
+  // the first request's index queries (B operand, SW128 layout)
+  const int first_req = cursor_at(p0, prefix, B).b;
+  {
+    const int R = rows_s[first_req], row0 = row0_s[first_req];
+    const int nrows = R * kGroups <= 16 ? 16 : 32;
+    for (int u = tid; u < nrows * 8; u += kThreads) {
+      const int nrow = u >> 3, ch = u & 7;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (nrow < R * kGroups)
+        v = *reinterpret_cast<const uint4*>(p.q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim + ch * 16);
+      *reinterpret_cast<uint4*>(sm.qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == kIssueWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.taddr;
   bool alive = true;
 
-  if (warp == kRowWarps) {
-    // ================= issue warp: TMA producer + MMA issuer (one lane)
+  if (warp == kLoadWarp) {
+    // ================= load warp: TMA producer (one lane)
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&ki_map)) : "memory");
       PageCursor ld = cursor_at(p0, prefix, B);
-      PageCursor mm = ld;
-      int issued = 0;
-      auto issue_load = [&](int i, const PageCursor& pc) {
+      for (int i = 0; i < n; ++i) {
         const int s = i % kStages;
-        const int phys = p.block_table[static_cast<long long>(pc.b) * p.max_pages + pc.c];
+        if (i >= kStages) {  // the dequant warps have released this stage's previous page
+          alive = wait_bar(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1, p.flags);
+          if (!alive) break;
+        }
+        const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(ld.b) * p.max_pages + ld.c];
         const bool bad = phys < 0 || phys >= p.num_pages;
         sm.stage_bad[s] = bad ? 1 : 0;
         const uint32_t bar = smem_u32(&sm.full[s]);
@@ -199,99 +307,147 @@ __global__ void __launch_bounds__(kThreads, 2)
           bulk_load(smem_u32(sm.scales[s]), p.ki_scale + static_cast<long long>(phys) * kScaleBytes, kScaleBytes,
                     bar);
         }
-      };
-      for (; issued < n && issued < kStages; ++issued) {
-        issue_load(issued, ld);
         cursor_advance(ld, nb);
-      }
-      for (int i = 0; i < n && alive; ++i) {
-        const int j = i & 1;
-        alive = mbar_wait(smem_u32(&sm.afull[j]), (i >> 1) & 1, p.flags);
-        if (alive && i >= 2) alive = mbar_wait(smem_u32(&sm.dempty[j]), ((i - 2) >> 1) & 1, p.flags);
-        if (!alive) break;
-        tc_fence_after();
-        const int R = rows_s[mm.b];
-        const int ncols = R * kGroups;
-        const int N = ncols <= 16 ? 16 : 32;
-        const uint32_t id_pos = idesc_e4m3_f32(128, N, false), id_neg = idesc_e4m3_f32(128, N, true);
-        const uint32_t d = tbase + kColD0 + 32 * j;
-        const uint32_t a = tbase + kColA0 + 64 * j;
-        const uint32_t qt = smem_u32(sm.qtile);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_f8_tmemA(d, a + 8 * k, sdesc_kmajor_sw128(qt + 32 * k), id_pos, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mma_f8_tmemA(d, a + 32 + 8 * k, sdesc_kmajor_sw128(qt + 32 * k), id_neg, 1);
-        mma_commit(smem_u32(&sm.dfull[j]));
-        cursor_advance(mm, nb);
-        if (issued < n) {
-          const int s = issued % kStages;
-          alive = mbar_wait(smem_u32(&sm.empty[s]), ((issued / kStages) - 1) & 1, p.flags);
-          if (!alive) break;
-          issue_load(issued, ld);
-          cursor_advance(ld, nb);
-          ++issued;
-        }
       }
       if (!alive) {
         // drain: copies already issued complete on their own barriers
-        for (int i = 0; i < issued; ++i) {
+        for (int i = 0; i < n; ++i) {
           const int s = i % kStages;
           if (!mbar_wait(smem_u32(&sm.full[s]), (i / kStages) & 1, p.flags)) break;
         }
       }
     }
     __syncwarp();
-  } else {
-    // ================= row warps: dequantise -> TMEM, epilogue
-    const int r = tid;  // token slot within the page = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    PageCursor cur = cursor_at(p0, prefix, B);
-    PageCursor prev = cur;
-    int qtile_req = -1;
-    bool cur_bad = false, prev_bad = false;  // page i / i-1 came from an out-of-range page id
-    for (int i = 0; i <= n && alive; ++i) {
-      uint32_t pa[32], na[32];
-      if (i < n) {
-        const int s = i % kStages;
-        alive = mbar_wait(smem_u32(&sm.full[s]), (i / kStages) & 1, p.flags);
-        if (!alive) break;
-        cur_bad = sm.stage_bad[s] != 0;  // read now: the stage is refilled once released
-        // this thread's row: 64 code bytes (swizzled 16-byte chunks) + 8 scale bytes
-        const uint8_t* row = sm.codes[s] + r * 64;
-        const int sw = (r >> 1) & 3;
-        uint4 cw[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) cw[c] = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
-        const uint2 scw = *reinterpret_cast<const uint2*>(sm.scales[s] + r * 8);
+  } else if (warp == kIssueWarp) {
+    // ================= MMA warp: MMA issue (lane 0), query tile (all lanes)
+    PageCursor mm = cursor_at(p0, prefix, B);
+    int qtile_req = first_req;
+    const uint32_t qt = smem_u32(sm.qtile);
+    for (int i = 0; i < n; ++i) {
+      const int j = i % kABufs, k = i % kDBufs;
+      if (mm.b != qtile_req) {
+        // new request: once every earlier MMA has finished reading the tile, rewrite it
+        if (i >= 1) alive = wait_bar(smem_u32(&sm.dfull[(i - 1) % kDBufs]), ((i - 1) / kDBufs) & 1, p.flags);
+        if (!__all_sync(0xFFFFFFFFu, alive)) {
+          alive = false;
+          break;
+        }
+        const int R = rows_s[mm.b], row0 = row0_s[mm.b];
+        const int nrows = R * kGroups <= 16 ? 16 : 32;
+        for (int u = lane; u < nrows * 8; u += 32) {
+          const int nrow = u >> 3, ch = u & 7;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (nrow < R * kGroups)
+            v = *reinterpret_cast<const uint4*>(p.q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim +
+                                                ch * 16);
+          *reinterpret_cast<uint4*>(sm.qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
-        const uint32_t w[16] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w, cw[1].x, cw[1].y, cw[1].z, cw[1].w,
-                                cw[2].x, cw[2].y, cw[2].z, cw[2].w, cw[3].x, cw[3].y, cw[3].z, cw[3].w};
+        qtile_req = mm.b;
+      }
+      if (lane == 0) {
+        alive = wait_bar(smem_u32(&sm.afull[j]), (i / kABufs) & 1, p.flags);
+        if (alive && i >= kDBufs) alive = wait_bar(smem_u32(&sm.dempty[k]), ((i / kDBufs) - 1) & 1, p.flags);
+        if (alive) {
+          tc_fence_after();
+          const int R = rows_s[mm.b];
+          const int N = R * kGroups <= 16 ? 16 : 32;
+          const uint32_t id_pos = idesc_e4m3_f32(128, N, false), id_neg = idesc_e4m3_f32(128, N, true);
+          const uint32_t d = tbase + kColD + 32 * k, a = tbase + kColA + 64 * j;
 #pragma unroll
-        for (int gsc = 0; gsc < 8; ++gsc) {  // 16-element group gsc = code words 2gsc, 2gsc+1
-          const uint32_t sb = ((gsc < 4 ? scw.x : scw.y) >> (8 * (gsc & 3))) & 0xFFu;
-          const LutEntry L = sm.lut[sb];
-          dq8_split(w[2 * gsc], L, pa[4 * gsc + 0], pa[4 * gsc + 1], na[4 * gsc + 0], na[4 * gsc + 1]);
-          dq8_split(w[2 * gsc + 1], L, pa[4 * gsc + 2], pa[4 * gsc + 3], na[4 * gsc + 2], na[4 * gsc + 3]);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_tmemA(d, a + 8 * kk, sdesc_kmajor_sw128(qt + 32 * kk), id_pos, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_tmemA(d, a + 32 + 8 * kk, sdesc_kmajor_sw128(qt + 32 * kk), id_neg, 1);
+          mma_commit(smem_u32(&sm.dfull[k]));
+          mma_commit(smem_u32(&sm.afree[j]));
         }
       }
-      // ---- epilogue of page i-1
-      if (i >= 1) {
-        const int jp = (i - 1) & 1;
-        alive = mbar_wait(smem_u32(&sm.dfull[jp]), ((i - 1) >> 1) & 1, p.flags);
+      cursor_advance(mm, nb);
+      if (!__all_sync(0xFFFFFFFFu, alive)) {
+        alive = false;
+        break;
+      }
+    }
+    __syncwarp();
+  } else if (warp < kRowWarps) {
+    // ================= dequant warps: page i -> TMEM A buffer i % kABufs
+    const int r = tid;  // token slot within the page = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kStages, j = i % kABufs;
+      uint32_t w[16];
+      alive = wait_bar(smem_u32(&sm.full[s]), (i / kStages) & 1, p.flags);
+      if (!alive) break;
+      // this thread's row: 64 code bytes (swizzled 16-byte chunks) + 8 scale bytes
+      const uint8_t* row = sm.codes[s] + r * 64;
+      const int sw = (r >> 1) & 3;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+        w[4 * c] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      const uint2 sc = *reinterpret_cast<const uint2*>(sm.scales[s] + r * 8);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
+      if (i >= kABufs) {  // the MMA that read this A buffer last time has finished
+        alive = wait_bar(smem_u32(&sm.afree[j]), ((i / kABufs) - 1) & 1, p.flags);
         if (!alive) break;
         tc_fence_after();
-        uint32_t dv[32];
-        tmem_ld32(tbase + lane_base + kColD0 + 32 * jp, dv);
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[jp]));
-        const int b = prev.b, c = prev.c;
-        const int N = ctx_s[b], R = rows_s[b], row0 = row0_s[b];
-        const int t = c * kBlock + r;
-        const bool page_bad = prev_bad;
-        float mg[kGroups] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      }
+      const uint32_t a_lane = tbase + lane_base + kColA + 64 * j;
+      dequant_store_half(sm.lut, w, sc.x, a_lane, a_lane + 32);
+      dequant_store_half(sm.lut, w + 8, sc.y, a_lane + 16, a_lane + 48);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.afull[j]));
+    }
+  } else {
+    // ================= epilogue warps: scores of page i from TMEM D buffer i % kDBufs
+    const int ew = warp - kRowWarps;  // 0..3: TMEM lanes 32ew..32ew+31 (warp % 4 == ew)
+    const int r = ew * 32 + lane;     // token slot within the page
+    const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
+    PageCursor cur = cursor_at(p0, prefix, B);
+    for (int i = 0; i < n; ++i) {
+      const int k = i % kDBufs;
+      alive = wait_bar(smem_u32(&sm.dfull[k]), (i / kDBufs) & 1, p.flags);
+      if (!alive) break;
+      tc_fence_after();
+      uint32_t dv[32];
+      tmem_ld32(tbase + lane_base + kColD + 32 * k, dv);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
+      const int b = cur.b, c = cur.c;
+      // the page's stage may already hold a later page: take the bad-id flag from the table
+      const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(b) * p.max_pages + c];
+      const bool page_bad = phys < 0 || phys >= p.num_pages;
+      const int N = ctx_s[b], R = rows_s[b];
+      const int t = c * kBlock + r;
+      float mg[kGroups];
+      if (MODE == 0 && !page_bad && c * kBlock + kBlock - 1 <= N - R) {
+        // every token of the page is visible to every row
+        switch (R) {
+          case 1: group_max<1>(dv, mg); break;
+          case 2: group_max<2>(dv, mg); break;
+          case 3: group_max<3>(dv, mg); break;
+          case 4: group_max<4>(dv, mg); break;
+          case 5: group_max<5>(dv, mg); break;
+          case 6: group_max<6>(dv, mg); break;
+          case 7: group_max<7>(dv, mg); break;
+          default: group_max<8>(dv, mg); break;
+        }
+      } else {
+        const int row0 = row0_s[b];
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) mg[g] = -INFINITY;
 #pragma unroll
         for (int rq = 0; rq < kMaxRows; ++rq) {
           if (rq < R) {
@@ -305,58 +461,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           }
         }
-        if (MODE == 0) {
-          // this warp's 32 tokens; the 4 warps' partial maxima of a block sit side
-          // by side and the top-k takes their max (no cross-warp barrier)
-#pragma unroll
-          for (int g = 0; g < kGroups; ++g) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mg[g] = fmaxf(mg[g], __shfl_xor_sync(0xFFFFFFFFu, mg[g], off));
-          }
+      }
+      if (MODE == 0) {
+        // this warp's 32 tokens, then the 4 epilogue warps' maxima merged in a
+        // shared-memory slot; the warp that completes the slot writes the block
+        // score and frees the slot (epilogue warps are at most 2 pages apart, so a
+        // ring of 4 slots never collides)
+        const float m0 = warp_max(mg[0]), m1 = warp_max(mg[1]), m2 = warp_max(mg[2]), m3 = warp_max(mg[3]);
+        const int slot = i & 3;
+        if (lane < kGroups) atomicMax(&sm.slot_max[slot][lane], ord_of(lane == 0 ? m0 : lane == 1 ? m1 : lane == 2 ? m2 : m3));
+        __threadfence_block();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&sm.slot_cnt[slot], 1) == kRowWarps - 1;
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (last) {
+          __threadfence_block();
           if (lane < kGroups) {
-            const float v = lane == 0 ? mg[0] : lane == 1 ? mg[1] : lane == 2 ? mg[2] : mg[3];
-            p.block_S[((static_cast<long long>(b) * kGroups + lane) * p.max_pages + c) * kRowWarps + warp] = v;
+            const int v = atomicExch(&sm.slot_max[slot][lane], INT_MIN);
+            p.block_S[(static_cast<long long>(b) * kGroups + lane) * p.s_stride + c] = float_of(v);
           }
+          __syncwarp();
+          if (lane == 0) atomicExch(&sm.slot_cnt[slot], 0);
         }
       }
-      prev = cur;
-      prev_bad = cur_bad;
-      if (i == n) break;
-      // ---- B operand: the request's index queries, rows n = rq*4 + g (SW128 layout)
-      if (cur.b != qtile_req) {
-        const int R = rows_s[cur.b], row0 = row0_s[cur.b];
-        const int nrows = R * kGroups <= 16 ? 16 : 32;
-        for (int u = r; u < nrows * 8; u += kRowWarps * 32) {
-          const int nrow = u >> 3, ch = u & 7;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (nrow < R * kGroups)
-            v = *reinterpret_cast<const uint4*>(p.q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim +
-                                                ch * 16);
-          *reinterpret_cast<uint4*>(sm.qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
-        qtile_req = cur.b;
-      }
-      // ---- A operand into TMEM: positive part cols [0,32), negative part [32,64)
-      const int j = i & 1;
-      const uint32_t a = tbase + lane_base + kColA0 + 64 * j;
-      uint32_t h[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) h[k] = pa[k];
-      tmem_st16(a, h);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) h[k] = pa[16 + k];
-      tmem_st16(a + 16, h);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) h[k] = na[k];
-      tmem_st16(a + 32, h);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) h[k] = na[16 + k];
-      tmem_st16(a + 48, h);
-      tc_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.afull[j]));
       cursor_advance(cur, nb);
     }
   }
@@ -364,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // ---- teardown
   tc_fence_before();
   const bool all_alive = __syncthreads_and(alive ? 1 : 0) != 0;
-  if (warp == kRowWarps) {
+  if (warp == kIssueWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -393,15 +521,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   __threadfence();
+  uint64_t* tk_scratch = reinterpret_cast<uint64_t*>(sm.codes[0]) + 64 * warp;  // stages are free now
   for (int k = 0; k < sm.ntodo; ++k) {
     const int b = todo[k];
     if (warp < kGroups) {
-      const float4* S = reinterpret_cast<const float4*>(p.block_S) +
-                        (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
-      warp_topk(S, nb[b], p.block_ids + (static_cast<long long>(b) * kGroups + warp) * kTopK);
+      const float* S = p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
+      warp_topk(S, nb[b], p.block_ids + (static_cast<long long>(b) * kGroups + warp) * kTopK, tk_scratch);
       if (p.block_scores_out != nullptr) {
         float* o = p.block_scores_out + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
-        for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nb[b] ? max4(S[c]) : -INFINITY;
+        for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nb[b] ? S[c] : -INFINITY;
       }
     }
   }
@@ -425,7 +553,7 @@ __global__ void __launch_bounds__(128) maxpool_topk_kernel(const MaxpoolParams p
     return;
   }
   const int nb = (N + kBlock - 1) / kBlock;
-  float4* S = reinterpret_cast<float4*>(p.block_S) + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
+  float* S = p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
   for (int c = 0; c < nb; ++c) {
     float m = -INFINITY;
     for (int rq = 0; rq < R; ++rq) {
@@ -438,13 +566,14 @@ __global__ void __launch_bounds__(128) maxpool_topk_kernel(const MaxpoolParams p
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    if (lane == 0) S[c] = make_float4(m, m, m, m);
+    if (lane == 0) S[c] = m;
   }
   __syncwarp();
-  warp_topk(S, nb, ids);
+  __shared__ uint64_t scratch[4][64];
+  warp_topk(S, nb, ids, scratch[warp]);
   if (p.block_scores_out != nullptr) {
     float* o = p.block_scores_out + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
-    for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nb ? max4(S[c]) : -INFINITY;
+    for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nb ? S[c] : -INFINITY;
   }
 }
 
@@ -490,8 +619,10 @@ size_t select_smem_bytes(int num_reqs) {
   return need > 80 * 1024 ? need : 80 * 1024;
 }
 
-cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int grid, cudaStream_t st) {
+cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,
+                          cudaStream_t st) {
   const size_t smem = select_smem_bytes(prm.num_reqs);
+  const int grid = kCtasPerSm * sm_count;
   cudaError_t e;
   if (mode == 0) {
     e = cudaFuncSetAttribute(select_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -164,8 +164,9 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* bl
  * (plugin / custom-operator interfaces), and for decode loops that must not call
  * cudaMalloc because it can synchronise the device. It runs the same kernel as
  * msa_select_blocks with the same outputs, but its scratch (error flags, arrival
- * counters, partial block maxima: 256 + 4*B + 64*B*max_pages_per_req bytes, rounded
- * up to 256) lives in a fixed 8 MiB device buffer inside the library, which every
+ * counters, block scores: 256 + 4*B rounded up to 256, plus 16*B*P4 bytes where P4 is
+ * max_pages_per_req rounded up to a multiple of 4) lives in a fixed 8 MiB device
+ * buffer inside the library, which every
  * GPU that loads libmsa holds until the process exits. Batches needing more return
  * MSA_ERR_WORKSPACE before any launch. It allocates nothing: the first call on each
  * device looks the buffer's address up once (make that first call before any
