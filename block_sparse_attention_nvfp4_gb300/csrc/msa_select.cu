@@ -10,26 +10,29 @@
 // FP8 MMA [vLLM-zh, Blackwell kernels].
 //
 // Design (GB300, sm_103a). Decode reads the whole index-key cache every step, so
-// this kernel is a stream over the cache's pages at HBM speed. One CTA has three
-// roles, 2 CTAs per SM (256 TMEM columns each), the grid taking equal contiguous
-// ranges of all requests' pages:
+// this kernel is a stream over the cache's pages at HBM speed. 2 CTAs per SM
+// (256 TMEM columns each), the grid taking equal contiguous ranges of all
+// requests' pages; one CTA has four roles:
 //   * load warp: one lane streams pages into a ring of shared-memory stages with
 //     TMA (codes: 2-D tensor copy with 64-byte swizzle, so each thread reads its
 //     64-byte row without bank conflicts; scales: 1-D bulk copy);
-//   * MMA warp: one lane issues the tensor-core MMAs (a single issuing thread
-//     sustains about one MMA per 45 cycles, so it does nothing else); the warp
-//     rewrites the index-query tile (B operand) when the request changes;
-//   * 4 dequant warps (thread = token of the page = TMEM lane): dequantise their
-//     token's 128 elements into positive/negative magnitude parts (byte-permute
-//     table lookups) and store them into a 3-deep ring of tensor-memory A
-//     buffers; the MMA computes scores = A x q_idx^T for the 4 x R index-query
-//     columns of the request, FP32 accumulation in tensor memory, the negative
-//     part through the negate-B bit (products of two E4M3 values are exact; only
-//     the FP32 sums round);
-//   * 4 epilogue warps: read each page's scores from a 2-deep ring of tensor-
-//     memory D buffers, mask, max-pool over the group's rows and their 32 tokens
-//     and write one partial per warp and block.
-// The dequant warps never wait for an MMA result, only for a free A buffer, so
+//   * 8 dequant warps in two groups that take alternate pages (thread = token):
+//     dequantise the token's 128 elements to E4M3 (byte-permute table lookups for
+//     magnitudes and signs) and write them as row `token` of a page tile in
+//     shared memory (the MMA's B operand, K-major, 128-byte swizzle);
+//   * MMA warp: one lane issues, per page, D = Q x P^T with Q the request's
+//     4 x R index-query rows (A operand, M = 128 of which rows >= 32 are never
+//     read back) and P the dequantised page (N = 128 tokens, K = 128), FP32
+//     accumulation in tensor memory (products of two E4M3 values are exact; only
+//     the FP32 sums round); the warp rewrites Q when the request changes;
+//   * 2 epilogue warps taking alternate pages (TMEM lanes 0..31 = the 32 query
+//     columns rq*4+g): read the page's 32 x 128 scores, mask, take each row's
+//     maximum over the tokens and the group's maximum over its rows with
+//     shuffles, and write the block score.
+// Laying the scores out with the query columns on TMEM lanes puts a whole page's
+// max pool in one warp (no cross-warp combine); measured on GB300, the pool was
+// the costliest step when the 128 tokens were spread over four warps' lanes.
+// The dequant warps never wait for an MMA result, only for a free page tile, so
 // the MMA round trip hides behind the next pages' dequantisation. The CTA that
 // completes a request's block scores (an arrival counter, no waiting) runs the
 // top-k for that request: one warp per group.
@@ -42,35 +45,41 @@ namespace msa {
 
 namespace {
 
-constexpr int kRowWarps = 4;                       // dequant warps = epilogue warps
-constexpr int kThreads = (2 * kRowWarps + 2) * 32;  // + the MMA warp + the TMA warp
-constexpr int kIssueWarp = 2 * kRowWarps;          // MMA issue, query tile
-constexpr int kLoadWarp = 2 * kRowWarps + 1;       // TMA producer
+// Warp roles. TMEM lanes 0..31 (the D rows read back) belong to warps with
+// warp % 4 == 0, so the two epilogue warps are 0 and 4 (page i -> warp 4 * (i % 2)).
+constexpr int kLoadWarp = 1;   // TMA producer
+constexpr int kIssueWarp = 2;  // MMA issue, query tile, TMEM allocation
+constexpr int kDqGroups = 2;   // page i is dequantised by group i % kDqGroups
+constexpr int kDqWarps = 4 * kDqGroups;  // warps 3, 5..11; 4 warps (128 tokens) per group
+constexpr int kThreads = 12 * 32;
+static_assert(kThreads == (4 + kDqWarps) * 32, "2 epilogue + load + MMA + dequant warps");
 constexpr int kCtasPerSm = 2;
-constexpr int kStages = 6;
-constexpr int kABufs = 3, kDBufs = 2;
+constexpr int kStages = 4, kBBufs = 3, kDBufs = 2;
 constexpr uint32_t kCodeBytes = kBlock * 64;    // one page of index-key codes
 constexpr uint32_t kScaleBytes = kBlock * 8;    // its scales
+constexpr uint32_t kTileBytes = kBlock * kDim;  // one dequantised page (E4M3)
 constexpr uint32_t kTmemCols = 256;
-constexpr int kCtaPages = 2048;                  // block-table entries staged per CTA
-// TMEM columns: kABufs A buffers (positive part 32 cols + negative part 32 cols),
-// then kDBufs D buffers (scores, up to 32 FP32 columns).
-constexpr uint32_t kColA = 0, kColD = 64 * kABufs;
+constexpr uint32_t kDCols = kBlock;             // D buffer: 128 FP32 columns (tokens)
+constexpr int kCtaPages = 2048;                 // block-table entries staged per CTA
+static_assert(kDBufs * kDCols <= kTmemCols, "TMEM buffers exceed the allocation");
 
 struct Smem {
+  // A operand: rows 0..31 hold the request's index queries. The MMA reads a
+  // 128-row tile, so rows 32..127 are the next 12 KB (the table and the staged
+  // block table, written once before the first MMA); their D lanes are never read.
+  uint8_t qtile[32 * 128];                  // offset 0
   LutEntry lut[256];                        // 4 KB
-  uint8_t codes[kStages][kCodeBytes];       // 1024-aligned (offset 4096)
-  uint8_t qtile[32 * 128];                  // B operand: up to 32 index-query rows x 128 (SW128)
+  int32_t phys[kCtaPages];                  // 8 KB: this CTA's block-table entries (when its range fits)
+  uint8_t codes[kStages][kCodeBytes];       // offset 16 KB, 1024-aligned
+  uint8_t tile[kBBufs][kTileBytes];         // B operand (SW128), 1024-aligned
   uint8_t scales[kStages][kScaleBytes];
   uint64_t full[kStages], empty[kStages];
-  uint64_t afull[kABufs], afree[kABufs], dfull[kDBufs], dempty[kDBufs];
-  int stage_bad[kStages];
-  int slot_max[4][kGroups];                 // per-page ring: ordered-int max of the epilogue warps' partials
-  int slot_cnt[4];                          // epilogue warps that have contributed to the slot
-  int32_t phys[kCtaPages];                  // this CTA's block-table entries (when its range fits)
+  uint64_t bfull[kBBufs], bfree[kBBufs], dfull[kDBufs], dempty[kDBufs];
   uint32_t taddr;
   int ntodo;
 };
+static_assert(sizeof(LutEntry) * 256 + sizeof(int32_t) * kCtaPages == 96 * 128,
+              "rows 32..127 of the A tile must cover the table and the staged block table exactly");
 
 struct PageCursor {
   int b;       // request
@@ -108,60 +117,57 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
   return m;
 }
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-// order-preserving int image of a float (for atomicMax), and back
-__device__ __forceinline__ int ord_of(float f) {
-  const int i = __float_as_int(f);
-  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
-}
-__device__ __forceinline__ float float_of(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7FFFFFFF)); }
 
-__device__ __forceinline__ uint32_t bitnot_fma(uint32_t w) {  // ~w on the multiply-add pipe
-  uint32_t r;
-  asm("mad.lo.u32 %0, %1, %2, %2;" : "=r"(r) : "r"(w), "r"(0xFFFFFFFFu));
-  return r;
-}
-
-// Group maxima of a fully visible token: columns n = rq*4 + g, rq < R.
-template <int R>
-__device__ __forceinline__ void group_max(const uint32_t (&dv)[32], float (&mg)[kGroups]) {
+// Maximum of 32 scores (one tcgen05 load): 4 independent chains.
+__device__ __forceinline__ float max32(const uint32_t (&v)[32]) {
+  float acc[4];
 #pragma unroll
-  for (int g = 0; g < kGroups; ++g) {
-    float m = __uint_as_float(dv[g]);
-#pragma unroll
-    for (int rq = 1; rq < R; rq += 2) {
-      const float a = __uint_as_float(dv[rq * kGroups + g]);
-      const float b = rq + 1 < R ? __uint_as_float(dv[(rq + 1) * kGroups + g]) : a;
-      m = fmax3(m, a, b);
-    }
-    mg[g] = m;
+  for (int u = 0; u < 4; ++u) {
+    float a = fmax3(__uint_as_float(v[u]), __uint_as_float(v[4 + u]), __uint_as_float(v[8 + u]));
+    a = fmax3(a, __uint_as_float(v[12 + u]), __uint_as_float(v[16 + u]));
+    a = fmax3(a, __uint_as_float(v[20 + u]), __uint_as_float(v[24 + u]));
+    acc[u] = fmaxf(a, __uint_as_float(v[28 + u]));
   }
+  return fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
 }
 
-// Dequantise 8 code words (4 groups of scale bytes sb0..sb3 = words 2k, 2k+1)
-// into 16 positive-part and 16 negative-part words and store them to TMEM.
-__device__ __forceinline__ void dequant_store_half(const LutEntry* lut, const uint32_t* w, uint32_t scw,
-                                                   uint32_t a_pos, uint32_t a_neg) {
-  uint32_t pa[16], na[16];
+// Maximum over the visible columns n <= lim of 32 scores starting at column n0.
+__device__ __forceinline__ float max32_masked(const uint32_t (&v)[32], int n0, int lim) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) m = fmaxf(m, n0 + u <= lim ? __uint_as_float(v[u]) : -INFINITY);
+  return m;
+}
+
+// Dequantise 8 code words (4 groups of 16 elements; scale byte q of scw belongs to
+// words 2q, 2q+1) to 64 signed E4M3 bytes and store them as 16-byte chunks
+// c0..c0+3 of a K-major SW128 row (chunk c of row r sits at chunk c ^ (r & 7)).
+__device__ __forceinline__ void dequant_half_to_tile(const LutEntry* lut, const uint32_t* w, uint32_t scw,
+                                                     uint32_t row_addr, int r7, int c0) {
+  uint32_t out[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const LutEntry L = lut[(scw >> (8 * q)) & 0xFFu];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t x = w[2 * q + h];
-      const uint32_t xh = x >> 16;
-      pa[4 * q + 2 * h] = prmt(L.p0, L.p1, x);
-      pa[4 * q + 2 * h + 1] = prmt(L.p0, L.p1, xh);
-      na[4 * q + 2 * h] = prmt(L.n0, L.n1, bitnot_fma(x));
-      na[4 * q + 2 * h + 1] = prmt(L.n0, L.n1, bitnot_fma(xh));
-    }
+    for (int h = 0; h < 2; ++h) dq8_signed(w[2 * q + h], L.p0, L.p1, out[4 * q + 2 * h], out[4 * q + 2 * h + 1]);
   }
-  tmem_st16(a_pos, pa);
-  tmem_st16(a_neg, na);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+    st_shared_v4(row_addr + (static_cast<uint32_t>((c0 + cc) ^ r7) << 4), out[4 * cc], out[4 * cc + 1],
+                 out[4 * cc + 2], out[4 * cc + 3]);
+}
+
+// Write the request's index-query rows (4 x R <= 32, zero rows after them) into
+// the A tile: row n = q_idx[row0 + n/4][group n%4], K-major with 128-byte swizzle.
+__device__ __forceinline__ void write_qtile(uint8_t* qtile, const uint8_t* q_idx, int row0, int R, int t0,
+                                            int nthreads) {
+  for (int u = t0; u < 32 * 8; u += nthreads) {
+    const int nrow = u >> 3, ch = u & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (nrow < R * kGroups)
+      v = *reinterpret_cast<const uint4*>(q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim + ch * 16);
+    *reinterpret_cast<uint4*>(qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
+  }
 }
 
 }  // namespace
@@ -206,14 +212,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   if (tid == 0) nb[B] = 1 << 30;  // sentinel stops cursor walks
   __syncthreads();
-  if (tid == 0) {  // B is at most a few thousand; a serial prefix is cheap
-    long long acc = 0;
-    for (int b = 0; b < B; ++b) {
+  if (warp == 0) {  // exclusive prefix over requests: each lane scans a contiguous chunk
+    const int per = (B + 31) / 32;
+    const int b0 = min(lane * per, B), b1 = min(b0 + per, B);
+    long long part = 0;
+    for (int b = b0; b < b1; ++b) part += nb[b];
+    long long incl = part;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    long long acc = incl - part;
+    for (int b = b0; b < b1; ++b) {
       prefix[b] = acc;
       acc += nb[b];
     }
-    prefix[B] = acc;
-    sm.ntodo = 0;
+    if (lane == 31) prefix[B] = incl;
+    if (lane == 0) sm.ntodo = 0;
   }
   __syncthreads();
   const long long total = prefix[B];
@@ -240,20 +256,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kRowWarps);
+      mbar_init(smem_u32(&sm.empty[s]), 4);  // the 4 warps of the page's dequant group
     }
-    for (int j = 0; j < kABufs; ++j) {
-      mbar_init(smem_u32(&sm.afull[j]), kRowWarps);
-      mbar_init(smem_u32(&sm.afree[j]), 1);
+    for (int j = 0; j < kBBufs; ++j) {
+      mbar_init(smem_u32(&sm.bfull[j]), 4);
+      mbar_init(smem_u32(&sm.bfree[j]), 1);
     }
     for (int k = 0; k < kDBufs; ++k) {
       mbar_init(smem_u32(&sm.dfull[k]), 1);
-      mbar_init(smem_u32(&sm.dempty[k]), kRowWarps);
+      mbar_init(smem_u32(&sm.dempty[k]), 1);
     }
     mbar_fence_init();
   }
-  if (tid < 4 * kGroups) sm.slot_max[tid / kGroups][tid % kGroups] = INT_MIN;
-  if (tid < 4) sm.slot_cnt[tid] = 0;
   // this CTA's block-table entries, so no page waits on a dependent global load
   const bool staged = n <= kCtaPages;
   if (staged) {
@@ -262,20 +276,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       sm.phys[i] = p.block_table[static_cast<long long>(pc.b) * p.max_pages + pc.c];
     }
   }
-  // the first request's index queries (B operand, SW128 layout)
+  // the first request's index queries
   const int first_req = cursor_at(p0, prefix, B).b;
-  {
-    const int R = rows_s[first_req], row0 = row0_s[first_req];
-    const int nrows = R * kGroups <= 16 ? 16 : 32;
-    for (int u = tid; u < nrows * 8; u += kThreads) {
-      const int nrow = u >> 3, ch = u & 7;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (nrow < R * kGroups)
-        v = *reinterpret_cast<const uint4*>(p.q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim + ch * 16);
-      *reinterpret_cast<uint4*>(sm.qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
-    }
-    fence_proxy_async_smem();
-  }
+  write_qtile(sm.qtile, p.q_idx, row0_s[first_req], rows_s[first_req], tid, kThreads);
+  fence_proxy_async_smem();
   if (warp == kIssueWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -290,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       PageCursor ld = cursor_at(p0, prefix, B);
       for (int i = 0; i < n; ++i) {
         const int s = i % kStages;
-        if (i >= kStages) {  // the dequant warps have released this stage's previous page
+
+        if (i >= kStages) {  // the dequant group has released this stage's previous page
           alive = wait_bar(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1, p.flags);
           if (!alive) break;
         }
         const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(ld.b) * p.max_pages + ld.c];
         const bool bad = phys < 0 || phys >= p.num_pages;
-        sm.stage_bad[s] = bad ? 1 : 0;
         const uint32_t bar = smem_u32(&sm.full[s]);
         if (bad) {
           set_flag(p.flags, kFlagBadPage);
@@ -322,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ================= MMA warp: MMA issue (lane 0), query tile (all lanes)
     PageCursor mm = cursor_at(p0, prefix, B);
     int qtile_req = first_req;
-    const uint32_t qt = smem_u32(sm.qtile);
+    // K step kk of an operand starts 32 bytes further: +2 in the start-address field
+    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
+    const uint32_t tile0 = smem_u32(sm.tile[0]);
+    const uint32_t idesc = idesc_e4m3_f32(128, kBlock, false);
     for (int i = 0; i < n; ++i) {
-      const int j = i % kABufs, k = i % kDBufs;
+      const int j = i % kBBufs, k = i % kDBufs;
       if (mm.b != qtile_req) {
         // new request: once every earlier MMA has finished reading the tile, rewrite it
         if (i >= 1) alive = wait_bar(smem_u32(&sm.dfull[(i - 1) % kDBufs]), ((i - 1) / kDBufs) & 1, p.flags);
@@ -332,37 +339,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           alive = false;
           break;
         }
-        const int R = rows_s[mm.b], row0 = row0_s[mm.b];
-        const int nrows = R * kGroups <= 16 ? 16 : 32;
-        for (int u = lane; u < nrows * 8; u += 32) {
-          const int nrow = u >> 3, ch = u & 7;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (nrow < R * kGroups)
-            v = *reinterpret_cast<const uint4*>(p.q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim +
-                                                ch * 16);
-          *reinterpret_cast<uint4*>(sm.qtile + nrow * 128 + ((ch ^ (nrow & 7)) << 4)) = v;
-        }
+        tc_fence_after();
+        write_qtile(sm.qtile, p.q_idx, row0_s[mm.b], rows_s[mm.b], lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         qtile_req = mm.b;
       }
       if (lane == 0) {
-        alive = wait_bar(smem_u32(&sm.afull[j]), (i / kABufs) & 1, p.flags);
+        alive = wait_bar(smem_u32(&sm.bfull[j]), (i / kBBufs) & 1, p.flags);
         if (alive && i >= kDBufs) alive = wait_bar(smem_u32(&sm.dempty[k]), ((i / kDBufs) - 1) & 1, p.flags);
         if (alive) {
           tc_fence_after();
-          const int R = rows_s[mm.b];
-          const int N = R * kGroups <= 16 ? 16 : 32;
-          const uint32_t id_pos = idesc_e4m3_f32(128, N, false), id_neg = idesc_e4m3_f32(128, N, true);
-          const uint32_t d = tbase + kColD + 32 * k, a = tbase + kColA + 64 * j;
+          const uint64_t bdesc = sdesc_kmajor_sw128(tile0 + j * kTileBytes);
+          const uint32_t d = tbase + k * kDCols;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_tmemA(d, a + 8 * kk, sdesc_kmajor_sw128(qt + 32 * kk), id_pos, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_tmemA(d, a + 32 + 8 * kk, sdesc_kmajor_sw128(qt + 32 * kk), id_neg, 1);
+          for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ss(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
           mma_commit(smem_u32(&sm.dfull[k]));
-          mma_commit(smem_u32(&sm.afree[j]));
+          mma_commit(smem_u32(&sm.bfree[j]));
         }
       }
       cursor_advance(mm, nb);
@@ -372,18 +365,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
     __syncwarp();
-  } else if (warp < kRowWarps) {
-    // ================= dequant warps: page i -> TMEM A buffer i % kABufs
-    const int r = tid;  // token slot within the page = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    for (int i = 0; i < n; ++i) {
-      const int s = i % kStages, j = i % kABufs;
+  } else if (warp != 0 && warp != 4) {
+    // ================= dequant warps: page i -> page tile i % kBBufs, by group i % kDqGroups
+    const int dw = warp == 3 ? 0 : warp - 4, grp = dw >> 2;
+    const int r = (dw & 3) * 32 + lane;  // token slot within the page = row of the page tile
+    const int r7 = r & 7, sw = (r >> 1) & 3;
+    const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + static_cast<uint32_t>(r7) * 128u;
+    const uint32_t tile0 = smem_u32(sm.tile[0]);
+    for (int i = grp; i < n; i += kDqGroups) {
+      const int s = i % kStages, j = i % kBBufs;
       uint32_t w[16];
       alive = wait_bar(smem_u32(&sm.full[s]), (i / kStages) & 1, p.flags);
       if (!alive) break;
       // this thread's row: 64 code bytes (swizzled 16-byte chunks) + 8 scale bytes
       const uint8_t* row = sm.codes[s] + r * 64;
-      const int sw = (r >> 1) & 3;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
@@ -395,96 +390,68 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint2 sc = *reinterpret_cast<const uint2*>(sm.scales[s] + r * 8);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[s]));
-      if (i >= kABufs) {  // the MMA that read this A buffer last time has finished
-        alive = wait_bar(smem_u32(&sm.afree[j]), ((i / kABufs) - 1) & 1, p.flags);
+      if (i >= kBBufs) {  // the MMAs that read this tile last time have finished
+        alive = wait_bar(smem_u32(&sm.bfree[j]), ((i / kBBufs) - 1) & 1, p.flags);
         if (!alive) break;
         tc_fence_after();
       }
-      const uint32_t a_lane = tbase + lane_base + kColA + 64 * j;
-      dequant_store_half(sm.lut, w, sc.x, a_lane, a_lane + 32);
-      dequant_store_half(sm.lut, w + 8, sc.y, a_lane + 16, a_lane + 48);
-      tc_wait_st();
-      tc_fence_before();
+      const uint32_t row_addr = tile0 + j * kTileBytes + row_off;
+      dequant_half_to_tile(sm.lut, w, sc.x, row_addr, r7, 0);
+      dequant_half_to_tile(sm.lut, w + 8, sc.y, row_addr, r7, 4);
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.afull[j]));
+      if (lane == 0) mbar_arrive(smem_u32(&sm.bfull[j]));
     }
   } else {
-    // ================= epilogue warps: scores of page i from TMEM D buffer i % kDBufs
-    const int ew = warp - kRowWarps;  // 0..3: TMEM lanes 32ew..32ew+31 (warp % 4 == ew)
-    const int r = ew * 32 + lane;     // token slot within the page
-    const uint32_t lane_base = static_cast<uint32_t>(ew * 32) << 16;
-    PageCursor cur = cursor_at(p0, prefix, B);
-    for (int i = 0; i < n; ++i) {
-      const int k = i % kDBufs;
+    // ================= epilogue warps 0 and 4: pages i = e, e + 2, ... (D buffer e);
+    // lane m = query column rq*4 + g of D
+    const int e = warp >> 2, rq = lane >> 2, g = lane & 3;
+    static_assert(kDBufs == 2, "one D buffer per epilogue warp");
+    PageCursor cur = cursor_at(p0 + (e < n ? e : 0), prefix, B);
+    for (int i = e; i < n; i += 2) {
+      const int k = e;
       alive = wait_bar(smem_u32(&sm.dfull[k]), (i / kDBufs) & 1, p.flags);
-      if (!alive) break;
+      if (!__all_sync(0xFFFFFFFFu, alive)) {
+        alive = false;
+        break;
+      }
       tc_fence_after();
-      uint32_t dv[32];
-      tmem_ld32(tbase + lane_base + kColD + 32 * k, dv);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
       const int b = cur.b, c = cur.c;
-      // the page's stage may already hold a later page: take the bad-id flag from the table
       const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(b) * p.max_pages + c];
       const bool page_bad = phys < 0 || phys >= p.num_pages;
       const int N = ctx_s[b], R = rows_s[b];
-      const int t = c * kBlock + r;
-      float mg[kGroups];
-      if (MODE == 0 && !page_bad && c * kBlock + kBlock - 1 <= N - R) {
-        // every token of the page is visible to every row
-        switch (R) {
-          case 1: group_max<1>(dv, mg); break;
-          case 2: group_max<2>(dv, mg); break;
-          case 3: group_max<3>(dv, mg); break;
-          case 4: group_max<4>(dv, mg); break;
-          case 5: group_max<5>(dv, mg); break;
-          case 6: group_max<6>(dv, mg); break;
-          case 7: group_max<7>(dv, mg); break;
-          default: group_max<8>(dv, mg); break;
-        }
-      } else {
-        const int row0 = row0_s[b];
+      const bool valid = rq < R && !page_bad;
+      const int t0 = c * kBlock;
+      const int lim = N - R + rq - t0;  // column n of this row is visible iff n <= lim
+      const uint32_t d = tbase + k * kDCols;
+      float m = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < kGroups; ++g) mg[g] = -INFINITY;
+      for (int q = 0; q < kBlock / 32; ++q) {
+        uint32_t v[32];
+        tmem_ld32(d + 32 * q, v);
+        tc_wait_ld();
+        if (MODE == 0) {
+          if (valid) m = fmaxf(m, lim >= kBlock - 1 ? max32(v) : max32_masked(v, 32 * q, lim));
+        } else if (rq < R) {
+          float* out = p.token_scores + (static_cast<long long>(row0_s[b] + rq) * kGroups + g) * p.score_stride + t0;
 #pragma unroll
-        for (int rq = 0; rq < kMaxRows; ++rq) {
-          if (rq < R) {
-            const bool vis = !page_bad && t <= N - R + rq;
-#pragma unroll
-            for (int g = 0; g < kGroups; ++g) {
-              const float v = vis ? __uint_as_float(dv[rq * kGroups + g]) : -INFINITY;
-              mg[g] = fmaxf(mg[g], v);
-              if (MODE == 1 && t < N)
-                p.token_scores[(static_cast<long long>(row0 + rq) * kGroups + g) * p.score_stride + t] = v;
-            }
+          for (int u = 0; u < 32; ++u) {
+            const int nn = 32 * q + u;
+            if (t0 + nn < N) out[nn] = valid && nn <= lim ? __uint_as_float(v[u]) : -INFINITY;
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
       if (MODE == 0) {
-        // this warp's 32 tokens, then the 4 epilogue warps' maxima merged in a
-        // shared-memory slot; the warp that completes the slot writes the block
-        // score and frees the slot (epilogue warps are at most 2 pages apart, so a
-        // ring of 4 slots never collides)
-        const float m0 = warp_max(mg[0]), m1 = warp_max(mg[1]), m2 = warp_max(mg[2]), m3 = warp_max(mg[3]);
-        const int slot = i & 3;
-        if (lane < kGroups) atomicMax(&sm.slot_max[slot][lane], ord_of(lane == 0 ? m0 : lane == 1 ? m1 : lane == 2 ? m2 : m3));
-        __threadfence_block();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&sm.slot_cnt[slot], 1) == kRowWarps - 1;
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last) {
-          __threadfence_block();
-          if (lane < kGroups) {
-            const int v = atomicExch(&sm.slot_max[slot][lane], INT_MIN);
-            p.block_S[(static_cast<long long>(b) * kGroups + lane) * p.s_stride + c] = float_of(v);
-          }
-          __syncwarp();
-          if (lane == 0) atomicExch(&sm.slot_cnt[slot], 0);
-        }
+        // the group's maximum over its rows: lanes with equal lane % 4
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        if (lane < kGroups) p.block_S[(static_cast<long long>(b) * kGroups + lane) * p.s_stride + c] = m;
       }
+      cursor_advance(cur, nb);
       cursor_advance(cur, nb);
     }
   }
