@@ -466,22 +466,51 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
   __threadfence();
   const int nsplit_used = (sm.nsel + p.blocks_per_split - 1) / p.blocks_per_split;
   const long long stride = static_cast<long long>(p.num_reqs) * kGroups * p.max_m;
-  for (int idx = tid; idx < M * kDim; idx += kAttnThreads) {
-    const int mrow = idx / kDim, d = idx % kDim;
+  // 1. per query row: the splits' weights exp2(lse2_s - ref) / sum, and the row's lse
+  float* wgt = &sm.u.comb_o[0][0][0];  // [M][kTopK], the block buffers are free now
+  for (int mrow = tid; mrow < M; mrow += kAttnThreads) {
     const long long base = static_cast<long long>(pair) * p.max_m + mrow;
+    float l2[kTopK];
     float mx = -INFINITY;
-    for (int s = 0; s < nsplit_used; ++s) mx = fmaxf(mx, p.part_lse2[s * stride + base]);
+#pragma unroll
+    for (int s = 0; s < kTopK; ++s) {
+      l2[s] = s < nsplit_used ? __ldcg(p.part_lse2 + s * stride + base) : -INFINITY;
+      mx = fmaxf(mx, l2[s]);
+    }
     const float ref = mx == -INFINITY ? 0.f : mx;
-    float num = 0.f, den = 0.f;
+    float den = 0.f;
+#pragma unroll
+    for (int s = 0; s < kTopK; ++s) {
+      l2[s] = s < nsplit_used ? exp2f(l2[s] - ref) : 0.f;
+      den += l2[s];
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+    for (int s = 0; s < kTopK; ++s) wgt[mrow * kTopK + s] = l2[s] * inv;
+    if (p.lse != nullptr) {
+      const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
+      p.lse[(static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh] =
+          den > 0.f ? (ref + log2f(den)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  __syncthreads();
+  // 2. out[row][4 dims] = sum over splits of weight x partial (16-byte loads, all threads)
+  for (int idx = tid; idx < M * (kDim / 4); idx += kAttnThreads) {
+    const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
+    const long long base = static_cast<long long>(pair) * p.max_m + mrow;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < nsplit_used; ++s) {
-      const float w = exp2f(p.part_lse2[s * stride + base] - ref);
-      den += w;
-      num += w * p.part_o[(s * stride + base) * kDim + d];
+      const float w = wgt[mrow * kTopK + s];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (s * stride + base) * kDim) + d4);
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
     }
     const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
     const long long orow = (static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh;
-    p.out[orow * kDim + d] = __bfloat16_as_ushort(__float2bfloat16_rn(den > 0.f ? num / den : 0.f));
-    if (d == 0 && p.lse != nullptr) p.lse[orow] = den > 0.f ? (ref + log2f(den)) * 0.69314718055994531f : -INFINITY;
+    uint2 packed = make_uint2(bf16x2_bits(acc.x, acc.y), bf16x2_bits(acc.z, acc.w));
+    *reinterpret_cast<uint2*>(p.out + orow * kDim + 4 * d4) = packed;
   }
 }
 
