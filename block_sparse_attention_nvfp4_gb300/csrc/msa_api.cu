@@ -18,9 +18,9 @@ namespace {
 constexpr size_t kWsAlign = 256;
 size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 
-int pow2_floor(int x) {
+int pow2_ceil(int x) {
   int p = 1;
-  while (p * 2 <= x) p *= 2;
+  while (p < x) p *= 2;
   return p;
 }
 
@@ -196,9 +196,11 @@ int score_stride(int max_pages) { return (max_pages + 3) / 4 * 4; }
 
 Plan make_plan(int num_reqs, int sm_count) {
   Plan pl;
+  // one attention CTA per SM: the fewest blocks per split that fit the (request,
+  // group) x split grid into one wave
   const int pairs = num_reqs * kGroups;
-  const int target = 2 * sm_count;
-  int bps = pairs > 0 ? pow2_floor((kTopK * pairs) / target) : kTopK;
+  const int target = sm_count > 0 ? sm_count : 1;
+  int bps = pairs > 0 ? pow2_ceil((kTopK * pairs + target - 1) / target) : kTopK;
   if (bps < 1) bps = 1;
   if (bps > kTopK) bps = kTopK;
   pl.blocks_per_split = bps;

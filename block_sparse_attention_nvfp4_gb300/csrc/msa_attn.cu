@@ -8,21 +8,25 @@
 // them. [vLLM-zh, Blackwell kernels] the K/V cache is NVFP4 and the queries FP8,
 // so K/V are turned into FP8 in the kernel and the products run as FP8 MMA.
 //
-// Design. Grid = (splits, request x group). A CTA takes `blocks_per_split` of
-// the group's selected blocks (flash-decoding split over the selection):
-//   * its 4 warps cooperatively dequantise each block's K (row-major FP8,
-//     k-step-interleaved, bank-swizzled) and V (transposed: dim-major, 4 keys per
-//     word) into shared memory, the raw NVFP4 pages double-buffered with bulk
-//     async copies;
-//   * each warp owns 16 query rows (row = speculative row x head) and a share of
-//     the block's keys: S = Q K^T with m16n8k32 FP8 MMA, FP32 online softmax,
-//     P rounded to E4M3 (scaled by 256 so small weights keep precision) feeding
-//     P V directly from the accumulator registers (the QK key order is chosen so
-//     its output fragment is the next MMA's input fragment);
-//   * warps that split a block's keys merge through shared memory; CTAs that
+// Design. Grid = (splits, request x group), one CTA per SM; a CTA takes
+// `blocks_per_split` of the group's selected blocks (flash-decoding split over
+// the selection), with warp roles so dequantisation and MMA overlap:
+//   * 4 dequant warps: the raw NVFP4 pages arrive in a 4-stage ring by bulk async
+//     copies; the warps dequantise each block's K (row-major FP8, k-step-
+//     interleaved, bank-swizzled) and V (transposed: dim-major, 4 keys per word)
+//     into one of two shared-memory tile buffers;
+//   * 4 MMA warps, each owning 16 query rows (row = speculative row x head) and
+//     a share of the block's keys: S = Q K^T with m16n8k32 FP8 MMA, FP32 online
+//     softmax, P rounded to E4M3 (scaled by 256 so small weights keep precision)
+//     feeding P V directly from the accumulator registers (the QK key order is
+//     chosen so its output fragment is the next MMA's input fragment);
+//   * MMA warps that split a block's keys merge through shared memory; CTAs that
 //     split the selection write (o, lse) partials and the last one to arrive for
 //     the (request, group) merges them with the exact log-sum-exp rule and
 //     writes BF16 output.
+// Measured on GB300, the earlier form (4 warps doing both, 2 CTAs per SM at 255
+// registers) spent about 3 us dequantising and 3.5 us attending per block, one
+// after the other, with each warp waiting on its own latencies.
 #include <cuda_bf16.h>
 
 #include "msa_common.cuh"
@@ -32,8 +36,12 @@ namespace msa {
 
 namespace {
 
-constexpr int kAttnThreads = 128;
-constexpr int kAttnStages = 2;
+constexpr int kMathWarps = 4;   // warps 0..3: MMA + softmax
+constexpr int kDqWarps = 4;     // warps 4..7: raw page copies + dequantisation
+constexpr int kAttnThreads = (kMathWarps + kDqWarps) * 32;
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kAttnStages = 4;  // raw NVFP4 page ring
+constexpr int kTileBufs = 2;    // dequantised K/V tiles
 constexpr uint32_t kHeadPageBytes = kBlock * 64;      // codes of one (page, KV head)
 constexpr uint32_t kHeadScaleBytes = kBlock * 8;
 
@@ -43,17 +51,15 @@ struct AttnSmem {
   uint8_t vc[kAttnStages][kHeadPageBytes];
   uint8_t ksc[kAttnStages][kHeadScaleBytes];
   uint8_t vsc[kAttnStages][kHeadScaleBytes];
-  union {
-    struct {
-      uint8_t khat[kBlock * kDim];            // [key][128], k-step slots swizzled
-      uint8_t vt[kDim * kBlock];              // [dim][128 keys], key slots swizzled
-    } blk;
-    float comb_o[4][16][kDim];                // key-split merge, after the last block
-  } u;
+  uint8_t khat[kTileBufs][kBlock * kDim];     // [key][128], k-step slots swizzled
+  uint8_t vt[kTileBufs][kDim * kBlock];       // [dim][128 keys], key slots swizzled
+  float comb_o[4][16][kDim];                  // key-split merge, then the split merge's weights
   float comb_ml[4][16][2];
-  uint64_t full[kAttnStages];
+  uint64_t full[kAttnStages], empty[kAttnStages];  // raw pages: copied / dequantised
+  uint64_t tfull[kTileBufs], tempty[kTileBufs];    // tiles: dequantised / consumed
   int stage_bad[kAttnStages];
   int ids[kTopK];
+  int phys[kTopK];                            // block-table entries of the selected blocks
   int nsel;
   int last;
 };
@@ -74,12 +80,13 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
 
 // Dequantise block (stage st) into khat / vt. Keys at or past `nvalid` get V = 0
 // (their weights are 0, and 0 * NaN from unwritten slots must not reach P V).
-__device__ __forceinline__ void dequant_block(AttnSmem& sm, int st, int nvalid, bool bad) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void dequant_block(AttnSmem& sm, int st, int buf, int nvalid, bool bad) {
+  const int tid = threadIdx.x - kMathWarps * 32;  // 0 .. kDqThreads-1
   // K: task = (key, 32-dim chunk) ; 8 consecutive threads read 128 contiguous bytes
-#pragma unroll 1
+  // (loops unrolled: the 4 tasks' loads and table lookups overlap)
+#pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int u = it * kAttnThreads + tid, key = u >> 2, ch = u & 3;
+    const int u = it * kDqThreads + tid, key = u >> 2, ch = u & 3;
     uint32_t x[8];
     if (!bad) {
       const uint4 cw = *reinterpret_cast<const uint4*>(sm.kc[st] + key * 64 + ch * 16);
@@ -94,14 +101,14 @@ __device__ __forceinline__ void dequant_block(AttnSmem& sm, int st, int nvalid, 
       for (int k = 0; k < 8; ++k) x[k] = 0u;
     }
     const int swz = ch ^ khat_swz(key);
-    uint8_t* row = sm.u.blk.khat + key * 128;
+    uint8_t* row = sm.khat[buf] + key * 128;
 #pragma unroll
     for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(row + (swz * 4 + t) * 8) = make_uint2(x[t], x[t + 4]);
   }
   // V: task = (4-key quad, 8-dim code word) -> transposed words (4 keys of one dim)
-#pragma unroll 1
+#pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int u = it * kAttnThreads + tid, q4 = u >> 4, wv = u & 15;
+    const int u = it * kDqThreads + tid, q4 = u >> 4, wv = u & 15;
     uint32_t y[4][2];
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
@@ -125,7 +132,7 @@ __device__ __forceinline__ void dequant_block(AttnSmem& sm, int st, int nvalid, 
 #pragma unroll
       for (int d4 = 0; d4 < 4; ++d4) {
         const int dim = 8 * wv + 4 * h + d4;
-        *reinterpret_cast<uint32_t*>(sm.u.blk.vt + dim * 128 + ((kk ^ (dim & 3)) * 4 + t) * 8 + boff) = z[d4];
+        *reinterpret_cast<uint32_t*>(sm.vt[buf] + dim * 128 + ((kk ^ (dim & 3)) * 4 + t) * 8 + boff) = z[d4];
       }
     }
   }
@@ -139,8 +146,9 @@ struct WarpState {
 
 // One block's keys [k0, k0 + 8*NT) for this warp's 16 rows.
 template <int NT>
-__device__ __forceinline__ void attend_keys(const AttnSmem& sm, WarpState& ws, const uint32_t (&qa)[4][4], int k0,
-                                            int blk_pos0, int posA, int posB, float scale_log2) {
+__device__ __forceinline__ void attend_keys(const uint8_t* khat, const uint8_t* vt, WarpState& ws,
+                                            const uint32_t (&qa)[4][4], int k0, int blk_pos0, int posA, int posB,
+                                            float scale_log2) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
   float s[NT][4];
 #pragma unroll
@@ -151,7 +159,7 @@ __device__ __forceinline__ void attend_keys(const AttnSmem& sm, WarpState& ws, c
   for (int j = 0; j < NT; ++j) {
     const int jl = j & 3;
     const int key = k0 + 32 * (j >> 2) + 16 * (jl >> 1) + 4 * (gq >> 1) + 2 * (jl & 1) + (gq & 1);
-    const uint8_t* row = sm.u.blk.khat + key * 128;
+    const uint8_t* row = khat + key * 128;
     const int hsw = khat_swz(key);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
@@ -222,7 +230,7 @@ __device__ __forceinline__ void attend_keys(const AttnSmem& sm, WarpState& ws, c
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
       const int dim = 8 * nd + gq;
-      const uint2 bv = *reinterpret_cast<const uint2*>(sm.u.blk.vt + dim * 128 + ((kk ^ (dim & 3)) * 4 + tq) * 8);
+      const uint2 bv = *reinterpret_cast<const uint2*>(vt + dim * 128 + ((kk ^ (dim & 3)) * 4 + tq) * 8);
       mma_m16n8k32(ws.o[nd], a0, a1, a2, a3, bv.x, bv.y);
     }
   }
@@ -231,39 +239,20 @@ __device__ __forceinline__ void attend_keys(const AttnSmem& sm, WarpState& ws, c
 template <int KWS>
 __device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int b, int g, int N, int r0, int R,
                                           int nmy, int jb0) {
-  constexpr int MTP = 4 / KWS;   // m-tiles covered by the 4 warps
+  constexpr int MTP = kMathWarps / KWS;  // m-tiles covered by the MMA warps
   constexpr int KPW = kBlock / KWS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int M = kQPerKV * R;
   const int MT = (M + 15) / 16;
   const int mt = warp % MTP, ksplit = warp / MTP;
-  const bool active = mt < MT;
+  const bool math = warp < kMathWarps;
+  const bool active = math && mt < MT;
   const int rA = 2 * mt, rB = 2 * mt + 1;  // speculative rows of this warp's two accumulator rows
   const int posA = N - R + rA, posB = N - R + rB;
 
-  uint32_t qa[4][4];
-  {
-    const uint8_t* qA = p.q + ((static_cast<long long>(r0 + rA) * kHeads) + kQPerKV * g + gq) * kDim;
-    const uint8_t* qB = p.q + ((static_cast<long long>(r0 + rB) * kHeads) + kQPerKV * g + gq) * kDim;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const bool okA = active && rA < R, okB = active && rB < R;
-      qa[ks][0] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 4 * tq) : 0u;
-      qa[ks][1] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 4 * tq) : 0u;
-      qa[ks][2] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 16 + 4 * tq) : 0u;
-      qa[ks][3] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 16 + 4 * tq) : 0u;
-    }
-  }
-  WarpState ws;
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) ws.o[nd][0] = ws.o[nd][1] = ws.o[nd][2] = ws.o[nd][3] = 0.f;
-  ws.mA = ws.mB = -INFINITY;
-  ws.lA = ws.lB = 0.f;
-
   auto issue = [&](int j) {
     const int st = j % kAttnStages;
-    const int blk = sm.ids[jb0 + j];
-    const int phys = p.block_table[static_cast<long long>(b) * p.max_pages + blk];
+    const int phys = sm.phys[jb0 + j];
     const uint32_t bar = smem_u32(&sm.full[st]);
     const bool bad = phys < 0 || phys >= p.num_pages;
     sm.stage_bad[st] = bad ? 1 : 0;
@@ -280,46 +269,81 @@ __device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int
     bulk_load(smem_u32(sm.vc[st]), p.v_data + head_row * 64, kHeadPageBytes, bar);
     bulk_load(smem_u32(sm.vsc[st]), p.v_scale + head_row * 8, kHeadScaleBytes, bar);
   };
-  if (tid == 0)
-    for (int j = 0; j < nmy && j < kAttnStages; ++j) issue(j);
 
-  bool alive = true;
-  for (int j = 0; j < nmy; ++j) {
-    const int st = j % kAttnStages;
-    alive = mbar_wait(smem_u32(&sm.full[st]), (j / kAttnStages) & 1, p.flags);
-    if (__syncthreads_or(alive ? 0 : 1)) {
-      alive = false;
-      break;
+  WarpState ws;
+  if (!math) {
+    // ================= dequant warps: raw page j (stage j % kAttnStages) -> tile j % kTileBufs
+    const int dtid = tid - kMathWarps * 32;
+    if (dtid == 0)
+      for (int j = 0; j < nmy && j < kAttnStages; ++j) issue(j);
+    for (int j = 0; j < nmy; ++j) {
+      const int st = j % kAttnStages, buf = j % kTileBufs;
+      if (!mbar_wait(smem_u32(&sm.full[st]), (j / kAttnStages) & 1, p.flags)) break;
+      if (j >= kTileBufs && !mbar_wait(smem_u32(&sm.tempty[buf]), ((j / kTileBufs) - 1) & 1, p.flags)) break;
+      const int blk = sm.ids[jb0 + j];
+      const int pos0 = blk * kBlock;
+      const int nvalid = N - pos0 < kBlock ? N - pos0 : kBlock;
+      dequant_block(sm, st, buf, nvalid, sm.stage_bad[st] != 0);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.tfull[buf]));
+        mbar_arrive(smem_u32(&sm.empty[st]));
+      }
+      // the stage's next page, once all 4 dequant warps have read this one
+      if (dtid == 0 && j + kAttnStages < nmy) {
+        if (!mbar_wait(smem_u32(&sm.empty[st]), (j / kAttnStages) & 1, p.flags)) break;
+        issue(j + kAttnStages);
+      }
     }
-    const int blk = sm.ids[jb0 + j];
-    const int pos0 = blk * kBlock;
-    const int nvalid = N - pos0 < kBlock ? N - pos0 : kBlock;
-    dequant_block(sm, st, nvalid, sm.stage_bad[st] != 0);
-    __syncthreads();
-    if (tid == 0 && j + kAttnStages < nmy) issue(j + kAttnStages);
-    if (active) {
-      constexpr int kChunk = KPW < 64 ? KPW : 64;  // keys per online-softmax step (register budget)
+  } else {
+    // ================= MMA warps
+    uint32_t qa[4][4];
+    {
+      const uint8_t* qA = p.q + ((static_cast<long long>(r0 + rA) * kHeads) + kQPerKV * g + gq) * kDim;
+      const uint8_t* qB = p.q + ((static_cast<long long>(r0 + rB) * kHeads) + kQPerKV * g + gq) * kDim;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const bool okA = active && rA < R, okB = active && rB < R;
+        qa[ks][0] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 4 * tq) : 0u;
+        qa[ks][1] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 4 * tq) : 0u;
+        qa[ks][2] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 16 + 4 * tq) : 0u;
+        qa[ks][3] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 16 + 4 * tq) : 0u;
+      }
+    }
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) ws.o[nd][0] = ws.o[nd][1] = ws.o[nd][2] = ws.o[nd][3] = 0.f;
+    ws.mA = ws.mB = -INFINITY;
+    ws.lA = ws.lB = 0.f;
+    for (int j = 0; j < nmy; ++j) {
+      const int buf = j % kTileBufs;
+      if (!mbar_wait(smem_u32(&sm.tfull[buf]), (j / kTileBufs) & 1, p.flags)) break;
+      if (active) {
+        const int pos0 = sm.ids[jb0 + j] * kBlock;
+        constexpr int kChunk = KPW < 64 ? KPW : 64;  // keys per online-softmax step (register budget)
 #pragma unroll 1
-      for (int kc = 0; kc < KPW; kc += kChunk)
-        attend_keys<kChunk / 8>(sm, ws, qa, ksplit * KPW + kc, pos0, posA, posB, p.sm_scale_log2);
+        for (int kc = 0; kc < KPW; kc += kChunk)
+          attend_keys<kChunk / 8>(sm.khat[buf], sm.vt[buf], ws, qa, ksplit * KPW + kc, pos0, posA, posB,
+                                  p.sm_scale_log2);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[buf]));
     }
   }
+  if (!math) return;  // the dequant warps are done; the MMA warps finish
   // full row sums across the quad
   ws.lA += __shfl_xor_sync(0xFFFFFFFFu, ws.lA, 1);
   ws.lA += __shfl_xor_sync(0xFFFFFFFFu, ws.lA, 2);
   ws.lB += __shfl_xor_sync(0xFFFFFFFFu, ws.lB, 1);
   ws.lB += __shfl_xor_sync(0xFFFFFFFFu, ws.lB, 2);
-  __syncthreads();  // khat / vt free: reuse as the merge buffer
-
   if (KWS > 1) {
     if (active && ksplit > 0) {
 #pragma unroll
       for (int nd = 0; nd < 16; ++nd) {
         const int d = 8 * nd + 2 * tq;
-        sm.u.comb_o[warp][gq][d] = ws.o[nd][0];
-        sm.u.comb_o[warp][gq][d + 1] = ws.o[nd][1];
-        sm.u.comb_o[warp][gq + 8][d] = ws.o[nd][2];
-        sm.u.comb_o[warp][gq + 8][d + 1] = ws.o[nd][3];
+        sm.comb_o[warp][gq][d] = ws.o[nd][0];
+        sm.comb_o[warp][gq][d + 1] = ws.o[nd][1];
+        sm.comb_o[warp][gq + 8][d] = ws.o[nd][2];
+        sm.comb_o[warp][gq + 8][d + 1] = ws.o[nd][3];
       }
       if (tq == 0) {
         sm.comb_ml[warp][gq][0] = ws.mA;
@@ -328,7 +352,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int
         sm.comb_ml[warp][gq + 8][1] = ws.lB;
       }
     }
-    __syncthreads();
+    named_bar_sync(1, kMathWarps * 32);  // the MMA warps only
     if (active && ksplit == 0) {
       float MA = ws.mA, MB = ws.mB;
 #pragma unroll
@@ -355,10 +379,10 @@ __device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int
 #pragma unroll
         for (int nd = 0; nd < 16; ++nd) {
           const int d = 8 * nd + 2 * tq;
-          ws.o[nd][0] += wA * sm.u.comb_o[w2][gq][d];
-          ws.o[nd][1] += wA * sm.u.comb_o[w2][gq][d + 1];
-          ws.o[nd][2] += wB * sm.u.comb_o[w2][gq + 8][d];
-          ws.o[nd][3] += wB * sm.u.comb_o[w2][gq + 8][d + 1];
+          ws.o[nd][0] += wA * sm.comb_o[w2][gq][d];
+          ws.o[nd][1] += wA * sm.comb_o[w2][gq][d + 1];
+          ws.o[nd][2] += wB * sm.comb_o[w2][gq + 8][d];
+          ws.o[nd][3] += wB * sm.comb_o[w2][gq + 8][d + 1];
         }
       }
       ws.mA = MA;
@@ -402,7 +426,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int
 
 }  // namespace
 
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem_al = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_al);
@@ -415,7 +439,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
                            cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16));
   }
   if (tid == 0) {
-    for (int s = 0; s < kAttnStages; ++s) mbar_init(smem_u32(&sm.full[s]), 1);
+    for (int s = 0; s < kAttnStages; ++s) {
+      mbar_init(smem_u32(&sm.full[s]), 1);
+      mbar_init(smem_u32(&sm.empty[s]), kDqWarps);
+    }
+    for (int t = 0; t < kTileBufs; ++t) {
+      mbar_init(smem_u32(&sm.tfull[t]), kDqWarps);
+      mbar_init(smem_u32(&sm.tempty[t]), kMathWarps);
+    }
     mbar_fence_init();
   }
 
@@ -442,6 +473,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
     sm.nsel = n;
   }
   __syncthreads();
+  // the selected blocks' page ids, read once (not on the copy-issue path)
+  if (tid < sm.nsel) sm.phys[tid] = p.block_table[static_cast<long long>(b) * p.max_pages + sm.ids[tid]];
+  __syncthreads();
   const int jb0 = blockIdx.x * p.blocks_per_split;
   int nmy = sm.nsel - jb0;
   nmy = nmy < 0 ? 0 : (nmy > p.blocks_per_split ? p.blocks_per_split : nmy);
@@ -467,7 +501,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnParams 
   const int nsplit_used = (sm.nsel + p.blocks_per_split - 1) / p.blocks_per_split;
   const long long stride = static_cast<long long>(p.num_reqs) * kGroups * p.max_m;
   // 1. per query row: the splits' weights exp2(lse2_s - ref) / sum, and the row's lse
-  float* wgt = &sm.u.comb_o[0][0][0];  // [M][kTopK], the block buffers are free now
+  float* wgt = &sm.comb_o[0][0][0];  // [M][kTopK], the block buffers are free now
   for (int mrow = tid; mrow < M; mrow += kAttnThreads) {
     const long long base = static_cast<long long>(pair) * p.max_m + mrow;
     float l2[kTopK];
