@@ -8,26 +8,38 @@
 // them. [vLLM-zh, Blackwell kernels] the K/V cache is NVFP4 and the queries FP8,
 // so K/V are turned into FP8 in the kernel and the products run as FP8 MMA.
 //
-// Design. Grid = (splits, request x group), one CTA per SM; a CTA takes
-// `blocks_per_split` of the group's selected blocks (flash-decoding split over
-// the selection), with warp roles so dequantisation and MMA overlap:
-//   * 4 dequant warps: the raw NVFP4 pages arrive in a 4-stage ring by bulk async
-//     copies; the warps dequantise each block's K (row-major FP8, k-step-
-//     interleaved, bank-swizzled) and V (transposed: dim-major, 4 keys per word)
-//     into one of two shared-memory tile buffers;
-//   * 4 MMA warps, each owning 16 query rows (row = speculative row x head) and
-//     a share of the block's keys: S = Q K^T with m16n8k32 FP8 MMA, FP32 online
-//     softmax, P rounded to E4M3 (scaled by 256 so small weights keep precision)
-//     feeding P V directly from the accumulator registers (the QK key order is
-//     chosen so its output fragment is the next MMA's input fragment);
-//   * MMA warps that split a block's keys merge through shared memory; CTAs that
-//     split the selection write (o, lse) partials and the last one to arrive for
-//     the (request, group) merges them with the exact log-sum-exp rule and
-//     writes BF16 output.
-// Measured on GB300, the earlier form (4 warps doing both, 2 CTAs per SM at 255
-// registers) spent about 3 us dequantising and 3.5 us attending per block, one
-// after the other, with each warp waiting on its own latencies.
+// Design (GB300, tcgen05). Grid = (splits, request x group), one CTA per SM; a
+// CTA takes `blocks_per_split` of the group's selected blocks (flash-decoding
+// split over the selection). The group's 8R query rows (R speculative rows x 8
+// heads, at most 64) are the rows of a 128-row MMA tile:
+//   * load warp: one lane copies each block's raw NVFP4 K and V (codes and
+//     scales) into a 4-stage shared-memory ring with bulk async copies;
+//   * 8 dequant warps, thread = one K row or one V row of the block: dequantise
+//     its 128 elements to E4M3 (byte-permute lookups in a table of scaled
+//     magnitudes) into a 128-byte-swizzled tile (V rows widened to FP16 into two
+//     64-dim tiles); two tile buffers;
+//   * MMA warp: one lane issues S = Q K^T (FP8; A = query tile, B = K tile, both
+//     shared memory, K-major) into one of two TMEM score buffers, and O += P V
+//     (FP16; A = P from TMEM, B = the V tile read MN-major, so V is used in its
+//     stored key-major order without a transpose, as two 64-dim halves) into the
+//     TMEM output;
+//   * 4 softmax warps, two per query row (TMEM lane), each with half of the row's
+//     keys and half of its output dims: read the 64 scores once into registers,
+//     mask, exchange the half maxima through shared memory, online softmax (FP32
+//     running max and sum; exp2 in packed FP16, two keys per instruction, which
+//     is also the FP16 form P takes as the next MMA's A operand in TMEM), and when
+//     the running max grows rescale the row's half of O in TMEM (after the
+//     previous P V has finished). S = Q K^T of block j+1 runs while block j's
+//     softmax does.
+// P V runs in FP16: the dequantised V values (E4M3) are exact in FP16, and an
+// E4M3 P (3 mantissa bits) measurably misses 2e-2 relative accuracy on rows whose
+// weight sits on a few keys; FP16 P keeps 11 bits.
+// CTAs that split the selection write (o, lse) partials and the last one to
+// arrive for the (request, group) merges them with the exact log-sum-exp rule and
+// writes BF16 output.
 #include <cuda_bf16.h>
+
+#include <cstddef>
 
 #include "msa_common.cuh"
 #include "msa_internal.h"
@@ -36,418 +48,129 @@ namespace msa {
 
 namespace {
 
-constexpr int kMathWarps = 4;   // warps 0..3: MMA + softmax
-constexpr int kDqWarps = 4;     // warps 4..7: raw page copies + dequantisation
-constexpr int kAttnThreads = (kMathWarps + kDqWarps) * 32;
-constexpr int kDqThreads = kDqWarps * 32;
-constexpr int kAttnStages = 4;  // raw NVFP4 page ring
-constexpr int kTileBufs = 2;    // dequantised K/V tiles
-constexpr uint32_t kHeadPageBytes = kBlock * 64;      // codes of one (page, KV head)
+// Warp w may access TMEM lanes 32 (w % 4) .. + 31; query rows are lanes 0..63.
+constexpr int kSoftWarps = 4;                       // warps 0, 1 (keys / dims 0..63), 4, 5 (64..127)
+constexpr int kMmaWarp = 2;                         // MMA issue, TMEM allocation
+constexpr int kLoadWarp = 3;                        // raw page copies
+constexpr int kDqWarp0 = 6, kDqWarps = 8;           // warps 6..13: K rows (0..127), V rows (128..255)
+constexpr int kAttnThreads = (kDqWarp0 + kDqWarps) * 32;
+constexpr int kAttnStages = 4;                      // raw NVFP4 page ring
+constexpr int kTileBufs = 2;                        // dequantised K / V tiles, TMEM score and P buffers
+constexpr uint32_t kHeadPageBytes = kBlock * 64;    // codes of one (page, KV head)
 constexpr uint32_t kHeadScaleBytes = kBlock * 8;
+constexpr uint32_t kTileBytes = kBlock * kDim;      // one dequantised K tile (E4M3, 128-byte rows)
+constexpr uint32_t kVHalfBytes = kBlock * 128;      // one V tile half: 128 keys x 64 dims FP16 (128-byte rows)
+constexpr int kLutCopies = 16;                      // one per thread of a 16-thread (8-byte) wavefront
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: S (2 x 128 FP32, one per key), O (128 FP32, one per dim), P (2 x 64,
+// 2 FP16 keys per column)
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+static_assert(kColP + 64 * kTileBufs <= kTmemCols, "TMEM buffers exceed the allocation");
+static_assert(kDqWarps * 32 == 2 * kBlock, "one dequant thread per K row and per V row");
 
 struct AttnSmem {
-  uint2 lut[256];                             // magnitude bytes of E2M1 codes 0..7 per scale
-  uint8_t kc[kAttnStages][kHeadPageBytes];
+  uint8_t qtile[128 * kDim];                        // A of S: query rows 0..M-1, zero rows after
+  uint8_t ktile[kTileBufs][kTileBytes];             // B of S (K-major): row = key
+  uint8_t vtile[kTileBufs][2][kVHalfBytes];         // B of O (MN-major, FP16): [half][key][64 dims]
+  uint8_t kc[kAttnStages][kHeadPageBytes];          // raw pages (bulk-copy destinations)
   uint8_t vc[kAttnStages][kHeadPageBytes];
   uint8_t ksc[kAttnStages][kHeadScaleBytes];
   uint8_t vsc[kAttnStages][kHeadScaleBytes];
-  uint8_t khat[kTileBufs][kBlock * kDim];     // [key][128], k-step slots swizzled
-  uint8_t vt[kTileBufs][kDim * kBlock];       // [dim][128 keys], key slots swizzled
-  float comb_o[4][16][kDim];                  // key-split merge, then the split merge's weights
-  float comb_ml[4][16][2];
-  uint64_t full[kAttnStages], empty[kAttnStages];  // raw pages: copied / dequantised
-  uint64_t tfull[kTileBufs], tempty[kTileBufs];    // tiles: dequantised / consumed
+  uint2 lut[128 * kLutCopies];                      // scaled magnitudes per scale magnitude, interleaved
+  float wgt[64 * kTopK];                            // split-merge weights
+  float xmax[2][64];                                // softmax halves' row maxima / sums
+  int soft_dead;                                    // a softmax warp gave up waiting
+  uint64_t raw_full[kAttnStages], raw_empty[kAttnStages];
+  uint64_t tile_full[kTileBufs], tile_free[kTileBufs];
+  uint64_t s_full[kTileBufs], s_free[kTileBufs], p_full[kTileBufs], o_done;
   int stage_bad[kAttnStages];
   int ids[kTopK];
-  int phys[kTopK];                            // block-table entries of the selected blocks
+  int phys[kTopK];                                  // block-table entries of the selected blocks
+  uint32_t taddr;
   int nsel;
   int last;
 };
-
-__device__ __forceinline__ int khat_swz(int key) { return (key & 1) | ((key >> 1) & 2); }
-
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
+static_assert(offsetof(AttnSmem, ktile) % 1024 == 0 && offsetof(AttnSmem, vtile) % 1024 == 0 &&
+                  kTileBytes % 1024 == 0 && kVHalfBytes % 1024 == 0,
+              "128-byte-swizzled MMA operands");
+static_assert(offsetof(AttnSmem, kc) % 16 == 0 && offsetof(AttnSmem, ksc) % 16 == 0 &&
+                  offsetof(AttnSmem, vsc) % 16 == 0 && kHeadScaleBytes % 16 == 0,
+              "bulk copies need 16-byte alignment");
+static_assert(offsetof(AttnSmem, raw_full) % 8 == 0, "mbarriers");
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
   const __nv_bfloat16 x = __float2bfloat16_rn(a), y = __float2bfloat16_rn(b);
   return static_cast<uint32_t>(__bfloat16_as_ushort(x)) | (static_cast<uint32_t>(__bfloat16_as_ushort(y)) << 16);
 }
 
-// Dequantise block (stage st) into khat / vt. Keys at or past `nvalid` get V = 0
-// (their weights are 0, and 0 * NaN from unwritten slots must not reach P V).
-__device__ __forceinline__ void dequant_block(AttnSmem& sm, int st, int buf, int nvalid, bool bad) {
-  const int tid = threadIdx.x - kMathWarps * 32;  // 0 .. kDqThreads-1
-  // K: task = (key, 32-dim chunk) ; 8 consecutive threads read 128 contiguous bytes
-  // (loops unrolled: the 4 tasks' loads and table lookups overlap)
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int u = it * kDqThreads + tid, key = u >> 2, ch = u & 3;
-    uint32_t x[8];
-    if (!bad) {
-      const uint4 cw = *reinterpret_cast<const uint4*>(sm.kc[st] + key * 64 + ch * 16);
-      const uint32_t sc = *reinterpret_cast<const uint16_t*>(sm.ksc[st] + key * 8 + 2 * ch);
-      const uint2 L0 = sm.lut[sc & 0xFFu], L1 = sm.lut[sc >> 8];
-      dq8_signed(cw.x, L0.x, L0.y, x[0], x[1]);
-      dq8_signed(cw.y, L0.x, L0.y, x[2], x[3]);
-      dq8_signed(cw.z, L1.x, L1.y, x[4], x[5]);
-      dq8_signed(cw.w, L1.x, L1.y, x[6], x[7]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = 0u;
-    }
-    const int swz = ch ^ khat_swz(key);
-    uint8_t* row = sm.khat[buf] + key * 128;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(row + (swz * 4 + t) * 8) = make_uint2(x[t], x[t + 4]);
-  }
-  // V: task = (4-key quad, 8-dim code word) -> transposed words (4 keys of one dim)
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int u = it * kDqThreads + tid, q4 = u >> 4, wv = u & 15;
-    uint32_t y[4][2];
-#pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-      const int key = 4 * q4 + k4;
-      if (!bad && key < nvalid) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(sm.vc[st] + key * 64 + wv * 4);
-        const uint2 L = sm.lut[sm.vsc[st][key * 8 + (wv >> 1)]];
-        dq8_signed(w, L.x, L.y, y[k4][0], y[k4][1]);
-      } else {
-        y[k4][0] = 0u;
-        y[k4][1] = 0u;
-      }
-    }
-    const int kk = q4 >> 3, tpos = q4 & 7, t = tpos & 3, boff = (tpos >> 2) * 4;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t t0 = __byte_perm(y[0][h], y[1][h], 0x5140), t1 = __byte_perm(y[0][h], y[1][h], 0x7362);
-      const uint32_t t2 = __byte_perm(y[2][h], y[3][h], 0x5140), t3 = __byte_perm(y[2][h], y[3][h], 0x7362);
-      const uint32_t z[4] = {__byte_perm(t0, t2, 0x5410), __byte_perm(t0, t2, 0x7632), __byte_perm(t1, t3, 0x5410),
-                             __byte_perm(t1, t3, 0x7632)};
-#pragma unroll
-      for (int d4 = 0; d4 < 4; ++d4) {
-        const int dim = 8 * wv + 4 * h + d4;
-        *reinterpret_cast<uint32_t*>(sm.vt[buf] + dim * 128 + ((kk ^ (dim & 3)) * 4 + t) * 8 + boff) = z[d4];
-      }
-    }
-  }
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t* flags) {
+  return mbar_try(bar, parity) || mbar_wait(bar, parity, flags);
 }
 
-// Per-warp attention state for 16 query rows: A = row gq, B = row gq + 8.
-struct WarpState {
-  float o[16][4];
-  float mA, mB, lA, lB;
-};
-
-// One block's keys [k0, k0 + 8*NT) for this warp's 16 rows.
-template <int NT>
-__device__ __forceinline__ void attend_keys(const uint8_t* khat, const uint8_t* vt, WarpState& ws,
-                                            const uint32_t (&qa)[4][4], int k0, int blk_pos0, int posA, int posB,
-                                            float scale_log2) {
-  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-  float s[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-  // S = Q K^T ; n-tile j of 32-key group kg = k0/32 + j/4 holds keys chosen so the
-  // accumulator layout equals the next MMA's A-operand layout
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int jl = j & 3;
-    const int key = k0 + 32 * (j >> 2) + 16 * (jl >> 1) + 4 * (gq >> 1) + 2 * (jl & 1) + (gq & 1);
-    const uint8_t* row = khat + key * 128;
-    const int hsw = khat_swz(key);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const uint2 bv = *reinterpret_cast<const uint2*>(row + (((ks ^ hsw) * 4) + tq) * 8);
-      mma_m16n8k32(s[j], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], bv.x, bv.y);
-    }
-  }
-  // mask + scale, row max
-  const bool need_mask = blk_pos0 + k0 + 8 * NT - 1 > (posA < posB ? posA : posB);
-  float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int jl = j & 3;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = k0 + 32 * (j >> 2) + 16 * (jl >> 1) + 4 * tq + 2 * (jl & 1) + e;
-      const int pos = blk_pos0 + key;
-      float a = s[j][e] * scale_log2, b = s[j][2 + e] * scale_log2;
-      if (need_mask) {
-        a = pos <= posA ? a : -INFINITY;
-        b = pos <= posB ? b : -INFINITY;
-      }
-      s[j][e] = a;
-      s[j][2 + e] = b;
-      mxA = fmaxf(mxA, a);
-      mxB = fmaxf(mxB, b);
-    }
-  }
-  mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 1));
-  mxA = fmaxf(mxA, __shfl_xor_sync(0xFFFFFFFFu, mxA, 2));
-  mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 1));
-  mxB = fmaxf(mxB, __shfl_xor_sync(0xFFFFFFFFu, mxB, 2));
-  const float nA = fmaxf(ws.mA, mxA), nB = fmaxf(ws.mB, mxB);
-  const float refA = nA == -INFINITY ? 0.f : nA, refB = nB == -INFINITY ? 0.f : nB;
-  const float alA = exp2f(ws.mA - refA), alB = exp2f(ws.mB - refB);
-  ws.mA = nA;
-  ws.mB = nB;
-  float sumA = 0.f, sumB = 0.f;
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    s[j][0] = exp2f(s[j][0] - refA);
-    s[j][1] = exp2f(s[j][1] - refA);
-    s[j][2] = exp2f(s[j][2] - refB);
-    s[j][3] = exp2f(s[j][3] - refB);
-    sumA += s[j][0] + s[j][1];
-    sumB += s[j][2] + s[j][3];
-  }
-  ws.lA = ws.lA * alA + sumA;
-  ws.lB = ws.lB * alB + sumB;
-#pragma unroll
-  for (int nd = 0; nd < 16; ++nd) {
-    ws.o[nd][0] *= alA;
-    ws.o[nd][1] *= alA;
-    ws.o[nd][2] *= alB;
-    ws.o[nd][3] *= alB;
-  }
-  // O += P V, P scaled by 256 and rounded to E4M3
-#pragma unroll
-  for (int kg = 0; kg < NT / 4; ++kg) {
-    const float f = 256.f;
-    const uint32_t a0 = pack_e4m3x4(s[4 * kg][0] * f, s[4 * kg][1] * f, s[4 * kg + 1][0] * f, s[4 * kg + 1][1] * f);
-    const uint32_t a1 = pack_e4m3x4(s[4 * kg][2] * f, s[4 * kg][3] * f, s[4 * kg + 1][2] * f, s[4 * kg + 1][3] * f);
-    const uint32_t a2 =
-        pack_e4m3x4(s[4 * kg + 2][0] * f, s[4 * kg + 2][1] * f, s[4 * kg + 3][0] * f, s[4 * kg + 3][1] * f);
-    const uint32_t a3 =
-        pack_e4m3x4(s[4 * kg + 2][2] * f, s[4 * kg + 2][3] * f, s[4 * kg + 3][2] * f, s[4 * kg + 3][3] * f);
-    const int kk = (k0 >> 5) + kg;
-#pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-      const int dim = 8 * nd + gq;
-      const uint2 bv = *reinterpret_cast<const uint2*>(vt + dim * 128 + ((kk ^ (dim & 3)) * 4 + tq) * 8);
-      mma_m16n8k32(ws.o[nd], a0, a1, a2, a3, bv.x, bv.y);
-    }
-  }
+// Dequantise code chunk k of a row (16 bytes = 32 elements; scale bytes 2k and
+// 2k+1 in the low 16 bits of s2) and store its 32 E4M3 bytes as chunks 2k, 2k+1
+// of the row in a 128-byte-swizzled tile (chunk c of row r sits at c ^ (r & 7)).
+__device__ __forceinline__ void dq_chunk(uint32_t lut_t, const uint4& v, uint32_t s2, uint32_t row_addr, int r7,
+                                         int k) {
+  const uint2 L0 = lds_u2(lut_t + ((s2 & 0x7Fu) << 7)), L1 = lds_u2(lut_t + (((s2 >> 8) & 0x7Fu) << 7));
+  uint32_t o[8];
+  dq8_signed(v.x, L0.x, L0.y, o[0], o[1]);
+  dq8_signed(v.y, L0.x, L0.y, o[2], o[3]);
+  dq8_signed(v.z, L1.x, L1.y, o[4], o[5]);
+  dq8_signed(v.w, L1.x, L1.y, o[6], o[7]);
+  st_shared_v4(row_addr + (static_cast<uint32_t>((2 * k) ^ r7) << 4), o[0], o[1], o[2], o[3]);
+  st_shared_v4(row_addr + (static_cast<uint32_t>((2 * k + 1) ^ r7) << 4), o[4], o[5], o[6], o[7]);
 }
 
-template <int KWS>
-__device__ __forceinline__ void attn_body(const AttnParams& p, AttnSmem& sm, int b, int g, int N, int r0, int R,
-                                          int nmy, int jb0) {
-  constexpr int MTP = kMathWarps / KWS;  // m-tiles covered by the MMA warps
-  constexpr int KPW = kBlock / KWS;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int M = kQPerKV * R;
-  const int MT = (M + 15) / 16;
-  const int mt = warp % MTP, ksplit = warp / MTP;
-  const bool math = warp < kMathWarps;
-  const bool active = math && mt < MT;
-  const int rA = 2 * mt, rB = 2 * mt + 1;  // speculative rows of this warp's two accumulator rows
-  const int posA = N - R + rA, posB = N - R + rB;
-
-  auto issue = [&](int j) {
-    const int st = j % kAttnStages;
-    const int phys = sm.phys[jb0 + j];
-    const uint32_t bar = smem_u32(&sm.full[st]);
-    const bool bad = phys < 0 || phys >= p.num_pages;
-    sm.stage_bad[st] = bad ? 1 : 0;
-    if (bad) {
-      set_flag(p.flags, kFlagBadPage);
-      mbar_arrive(bar);
-      return;
-    }
-    const long long head_row = (static_cast<long long>(phys) * kGroups + g) * kBlock;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, 2 * (kHeadPageBytes + kHeadScaleBytes));
-    bulk_load(smem_u32(sm.kc[st]), p.k_data + head_row * 64, kHeadPageBytes, bar);
-    bulk_load(smem_u32(sm.ksc[st]), p.k_scale + head_row * 8, kHeadScaleBytes, bar);
-    bulk_load(smem_u32(sm.vc[st]), p.v_data + head_row * 64, kHeadPageBytes, bar);
-    bulk_load(smem_u32(sm.vsc[st]), p.v_scale + head_row * 8, kHeadScaleBytes, bar);
-  };
-
-  WarpState ws;
-  if (!math) {
-    // ================= dequant warps: raw page j (stage j % kAttnStages) -> tile j % kTileBufs
-    const int dtid = tid - kMathWarps * 32;
-    if (dtid == 0)
-      for (int j = 0; j < nmy && j < kAttnStages; ++j) issue(j);
-    for (int j = 0; j < nmy; ++j) {
-      const int st = j % kAttnStages, buf = j % kTileBufs;
-      if (!mbar_wait(smem_u32(&sm.full[st]), (j / kAttnStages) & 1, p.flags)) break;
-      if (j >= kTileBufs && !mbar_wait(smem_u32(&sm.tempty[buf]), ((j / kTileBufs) - 1) & 1, p.flags)) break;
-      const int blk = sm.ids[jb0 + j];
-      const int pos0 = blk * kBlock;
-      const int nvalid = N - pos0 < kBlock ? N - pos0 : kBlock;
-      dequant_block(sm, st, buf, nvalid, sm.stage_bad[st] != 0);
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.tfull[buf]));
-        mbar_arrive(smem_u32(&sm.empty[st]));
-      }
-      // the stage's next page, once all 4 dequant warps have read this one
-      if (dtid == 0 && j + kAttnStages < nmy) {
-        if (!mbar_wait(smem_u32(&sm.empty[st]), (j / kAttnStages) & 1, p.flags)) break;
-        issue(j + kAttnStages);
-      }
-    }
-  } else {
-    // ================= MMA warps
-    uint32_t qa[4][4];
-    {
-      const uint8_t* qA = p.q + ((static_cast<long long>(r0 + rA) * kHeads) + kQPerKV * g + gq) * kDim;
-      const uint8_t* qB = p.q + ((static_cast<long long>(r0 + rB) * kHeads) + kQPerKV * g + gq) * kDim;
+// V row variant: the 32 E4M3 values of code chunk k widened to FP16 (exact) and
+// stored as FP16 chunks 4(k & 1) .. 4(k & 1) + 3 of the row in V half k / 2.
+__device__ __forceinline__ void dq_chunk_v(uint32_t lut_t, const uint4& v, uint32_t s2, uint32_t half_row0,
+                                           int r7, int k) {
+  const uint2 L0 = lds_u2(lut_t + ((s2 & 0x7Fu) << 7)), L1 = lds_u2(lut_t + (((s2 >> 8) & 0x7Fu) << 7));
+  uint32_t o[8];
+  dq8_signed(v.x, L0.x, L0.y, o[0], o[1]);
+  dq8_signed(v.y, L0.x, L0.y, o[2], o[3]);
+  dq8_signed(v.z, L1.x, L1.y, o[4], o[5]);
+  dq8_signed(v.w, L1.x, L1.y, o[6], o[7]);
+  uint32_t h[16];
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const bool okA = active && rA < R, okB = active && rB < R;
-        qa[ks][0] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 4 * tq) : 0u;
-        qa[ks][1] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 4 * tq) : 0u;
-        qa[ks][2] = okA ? *reinterpret_cast<const uint32_t*>(qA + 32 * ks + 16 + 4 * tq) : 0u;
-        qa[ks][3] = okB ? *reinterpret_cast<const uint32_t*>(qB + 32 * ks + 16 + 4 * tq) : 0u;
-      }
-    }
-#pragma unroll
-    for (int nd = 0; nd < 16; ++nd) ws.o[nd][0] = ws.o[nd][1] = ws.o[nd][2] = ws.o[nd][3] = 0.f;
-    ws.mA = ws.mB = -INFINITY;
-    ws.lA = ws.lB = 0.f;
-    for (int j = 0; j < nmy; ++j) {
-      const int buf = j % kTileBufs;
-      if (!mbar_wait(smem_u32(&sm.tfull[buf]), (j / kTileBufs) & 1, p.flags)) break;
-      if (active) {
-        const int pos0 = sm.ids[jb0 + j] * kBlock;
-        constexpr int kChunk = KPW < 64 ? KPW : 64;  // keys per online-softmax step (register budget)
-#pragma unroll 1
-        for (int kc = 0; kc < KPW; kc += kChunk)
-          attend_keys<kChunk / 8>(sm.khat[buf], sm.vt[buf], ws, qa, ksplit * KPW + kc, pos0, posA, posB,
-                                  p.sm_scale_log2);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.tempty[buf]));
-    }
+  for (int i = 0; i < 8; ++i) {
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h[2 * i]) : "r"(o[i] & 0xFFFFu));
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h[2 * i + 1]) : "r"(o[i] >> 16));
   }
-  if (!math) return;  // the dequant warps are done; the MMA warps finish
-  // full row sums across the quad
-  ws.lA += __shfl_xor_sync(0xFFFFFFFFu, ws.lA, 1);
-  ws.lA += __shfl_xor_sync(0xFFFFFFFFu, ws.lA, 2);
-  ws.lB += __shfl_xor_sync(0xFFFFFFFFu, ws.lB, 1);
-  ws.lB += __shfl_xor_sync(0xFFFFFFFFu, ws.lB, 2);
-  if (KWS > 1) {
-    if (active && ksplit > 0) {
+  const uint32_t row = half_row0 + static_cast<uint32_t>(k >> 1) * kVHalfBytes;
 #pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        const int d = 8 * nd + 2 * tq;
-        sm.comb_o[warp][gq][d] = ws.o[nd][0];
-        sm.comb_o[warp][gq][d + 1] = ws.o[nd][1];
-        sm.comb_o[warp][gq + 8][d] = ws.o[nd][2];
-        sm.comb_o[warp][gq + 8][d + 1] = ws.o[nd][3];
-      }
-      if (tq == 0) {
-        sm.comb_ml[warp][gq][0] = ws.mA;
-        sm.comb_ml[warp][gq][1] = ws.lA;
-        sm.comb_ml[warp][gq + 8][0] = ws.mB;
-        sm.comb_ml[warp][gq + 8][1] = ws.lB;
-      }
-    }
-    named_bar_sync(1, kMathWarps * 32);  // the MMA warps only
-    if (active && ksplit == 0) {
-      float MA = ws.mA, MB = ws.mB;
-#pragma unroll
-      for (int k = 1; k < KWS; ++k) {
-        MA = fmaxf(MA, sm.comb_ml[warp + k * MTP][gq][0]);
-        MB = fmaxf(MB, sm.comb_ml[warp + k * MTP][gq + 8][0]);
-      }
-      const float refA = MA == -INFINITY ? 0.f : MA, refB = MB == -INFINITY ? 0.f : MB;
-      const float wA0 = exp2f(ws.mA - refA), wB0 = exp2f(ws.mB - refB);
-      float lA = ws.lA * wA0, lB = ws.lB * wB0;
-#pragma unroll
-      for (int nd = 0; nd < 16; ++nd) {
-        ws.o[nd][0] *= wA0;
-        ws.o[nd][1] *= wA0;
-        ws.o[nd][2] *= wB0;
-        ws.o[nd][3] *= wB0;
-      }
-#pragma unroll
-      for (int k = 1; k < KWS; ++k) {
-        const int w2 = warp + k * MTP;
-        const float wA = exp2f(sm.comb_ml[w2][gq][0] - refA), wB = exp2f(sm.comb_ml[w2][gq + 8][0] - refB);
-        lA += sm.comb_ml[w2][gq][1] * wA;
-        lB += sm.comb_ml[w2][gq + 8][1] * wB;
-#pragma unroll
-        for (int nd = 0; nd < 16; ++nd) {
-          const int d = 8 * nd + 2 * tq;
-          ws.o[nd][0] += wA * sm.comb_o[w2][gq][d];
-          ws.o[nd][1] += wA * sm.comb_o[w2][gq][d + 1];
-          ws.o[nd][2] += wB * sm.comb_o[w2][gq + 8][d];
-          ws.o[nd][3] += wB * sm.comb_o[w2][gq + 8][d + 1];
-        }
-      }
-      ws.mA = MA;
-      ws.mB = MB;
-      ws.lA = lA;
-      ws.lB = lB;
-    }
-  }
-
-  // ---- write: final (single split) or partial for the merge
-  const int pair = b * kGroups + g;
-  if (active && ksplit == 0) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int rq = half ? rB : rA;
-      const float m = half ? ws.mB : ws.mA, l = half ? ws.lB : ws.lA;
-      if (rq >= R) continue;
-      const int mrow = rq * kQPerKV + gq;  // query row within the pair
-      const float inv = l > 0.f ? 1.f / (256.f * l) : 0.f;
-      const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
-      if (p.splits == 1) {
-        uint32_t* out = reinterpret_cast<uint32_t*>(p.out + ((static_cast<long long>(r0 + rq) * kHeads) +
-                                                            kQPerKV * g + gq) * kDim);
-#pragma unroll
-        for (int nd = 0; nd < 16; ++nd)
-          out[(8 * nd + 2 * tq) >> 1] = bf16x2_bits(ws.o[nd][2 * half] * inv, ws.o[nd][2 * half + 1] * inv);
-        if (p.lse != nullptr && tq == 0)
-          p.lse[(static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + gq] = lse2 * 0.69314718055994531f;
-      } else {
-        const long long base =
-            ((static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m + mrow);
-        float2* po = reinterpret_cast<float2*>(p.part_o + base * kDim);
-#pragma unroll
-        for (int nd = 0; nd < 16; ++nd)
-          po[(8 * nd + 2 * tq) >> 1] = make_float2(ws.o[nd][2 * half] * inv, ws.o[nd][2 * half + 1] * inv);
-        if (tq == 0) p.part_lse2[base] = lse2;
-      }
-    }
-  }
+  for (int cc = 0; cc < 4; ++cc)
+    st_shared_v4(row + (static_cast<uint32_t>((4 * (k & 1) + cc) ^ r7) << 4), h[4 * cc], h[4 * cc + 1], h[4 * cc + 2],
+                 h[4 * cc + 3]);
 }
 
 }  // namespace
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem_al = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  uint8_t* smem_al = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // swizzled tiles: 1 KB
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>(smem_al);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pair = blockIdx.y, b = pair / kGroups, g = pair % kGroups;
 
-  for (int s = tid; s < 256; s += kAttnThreads) {
-    const uint32_t sc = e4m3_to_h2_bcast(static_cast<uint32_t>(s & 0x7F));
-    sm.lut[s] = make_uint2(cvt_e2m1x2_scaled(0x10, sc) | (cvt_e2m1x2_scaled(0x32, sc) << 16),
-                           cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16));
-  }
+  for (int u = tid; u < 128 * kLutCopies; u += kAttnThreads)
+    sm.lut[u] = lut_magnitudes(static_cast<uint32_t>(u / kLutCopies));
   if (tid == 0) {
     for (int s = 0; s < kAttnStages; ++s) {
-      mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kDqWarps);
+      mbar_init(smem_u32(&sm.raw_full[s]), 1);
+      mbar_init(smem_u32(&sm.raw_empty[s]), kDqWarps);
     }
     for (int t = 0; t < kTileBufs; ++t) {
-      mbar_init(smem_u32(&sm.tfull[t]), kDqWarps);
-      mbar_init(smem_u32(&sm.tempty[t]), kMathWarps);
+      mbar_init(smem_u32(&sm.tile_full[t]), kDqWarps);
+      mbar_init(smem_u32(&sm.tile_free[t]), 1);
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.s_free[t]), kSoftWarps);
+      mbar_init(smem_u32(&sm.p_full[t]), kSoftWarps);
     }
+    mbar_init(smem_u32(&sm.o_done), 1);
     mbar_fence_init();
+    sm.soft_dead = 0;
   }
 
   // block ids are produced by the preceding selection kernel
@@ -475,16 +198,302 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   __syncthreads();
   // the selected blocks' page ids, read once (not on the copy-issue path)
   if (tid < sm.nsel) sm.phys[tid] = p.block_table[static_cast<long long>(b) * p.max_pages + sm.ids[tid]];
+  const int M = kQPerKV * R;  // query rows of this (request, group): row m = speculative row m/8, head m%8
+  // query tile: 128 rows x 128 bytes, 128-byte swizzle; rows >= M are zero
+  for (int u = tid; u < 128 * 8; u += kAttnThreads) {
+    const int m = u >> 3, ch = u & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v = *reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<long long>(r0 + m / kQPerKV) * kHeads) + kQPerKV * g + m % kQPerKV) * kDim + ch * 16);
+    *reinterpret_cast<uint4*>(sm.qtile + m * 128 + ((ch ^ (m & 7)) << 4)) = v;
+  }
+  fence_proxy_async_smem();
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.taddr;
   const int jb0 = blockIdx.x * p.blocks_per_split;
   int nmy = sm.nsel - jb0;
   nmy = nmy < 0 ? 0 : (nmy > p.blocks_per_split ? p.blocks_per_split : nmy);
 
-  const int M = kQPerKV * R;
-  const int MT = (M + 15) / 16;
-  if (MT == 1) attn_body<4>(p, sm, b, g, N, r0, R, nmy, jb0);
-  else if (MT == 2) attn_body<2>(p, sm, b, g, N, r0, R, nmy, jb0);
-  else attn_body<1>(p, sm, b, g, N, r0, R, nmy, jb0);
+  if (warp == kLoadWarp) {
+    // ================= load warp: raw K/V pages of block j into stage j % kAttnStages
+    if (lane == 0) {
+      auto issue = [&](int j) {
+        const int st = j % kAttnStages;
+        const int phys = sm.phys[jb0 + j];
+        const uint32_t bar = smem_u32(&sm.raw_full[st]);
+        const bool bad = phys < 0 || phys >= p.num_pages;
+        sm.stage_bad[st] = bad ? 1 : 0;
+        if (bad) {
+          set_flag(p.flags, kFlagBadPage);
+          mbar_arrive(bar);
+          return;
+        }
+        const long long head_row = (static_cast<long long>(phys) * kGroups + g) * kBlock;
+        mbar_arrive_expect_tx(bar, 2 * (kHeadPageBytes + kHeadScaleBytes));
+        bulk_load(smem_u32(sm.kc[st]), p.k_data + head_row * 64, kHeadPageBytes, bar);
+        bulk_load(smem_u32(sm.ksc[st]), p.k_scale + head_row * 8, kHeadScaleBytes, bar);
+        bulk_load(smem_u32(sm.vc[st]), p.v_data + head_row * 64, kHeadPageBytes, bar);
+        bulk_load(smem_u32(sm.vsc[st]), p.v_scale + head_row * 8, kHeadScaleBytes, bar);
+      };
+      for (int j = 0; j < nmy && j < kAttnStages; ++j) issue(j);
+      for (int j = kAttnStages; j < nmy; ++j) {
+        const int st = j % kAttnStages;
+        if (!wait_bar(smem_u32(&sm.raw_empty[st]), ((j / kAttnStages) - 1) & 1, p.flags)) break;
+        issue(j);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kDqWarp0) {
+    // ================= dequant warps: thread t = K row t (t < 128) or V row t - 128
+    const int t = tid - kDqWarp0 * 32;
+    const bool is_v = t >= kBlock;
+    const int r = t & (kBlock - 1), r7 = r & 7;
+    // chunk order k = c ^ h((r >> 1) & 3), h = multiplication by a generator of GF(4)
+    // (0,1,2,3 -> 0,2,3,1): both h and x ^ h(x) are permutations, so the 8 rows of a
+    // shared-memory wavefront hit 8 different 16-byte bank groups on the 64-byte code
+    // reads (slot (r & 1) * 4 + k) and on the tile writes (slot 2k ^ (r & 7))
+    const int h = (0x78 >> (2 * ((r >> 1) & 3))) & 3;
+    const uint32_t lut_t = smem_u32(sm.lut) + static_cast<uint32_t>(lane % kLutCopies) * 8u;
+    for (int j = 0; j < nmy; ++j) {
+      const int st = j % kAttnStages, buf = j % kTileBufs;
+      if (!wait_bar(smem_u32(&sm.raw_full[st]), (j / kAttnStages) & 1, p.flags)) break;
+      if (j >= kTileBufs && !wait_bar(smem_u32(&sm.tile_free[buf]), ((j / kTileBufs) - 1) & 1, p.flags)) break;
+      const int pos0 = sm.ids[jb0 + j] * kBlock;
+      const int nvalid = N - pos0 < kBlock ? N - pos0 : kBlock;
+      const uint32_t row_addr = smem_u32(is_v ? sm.vtile[buf][0] : sm.ktile[buf]) + static_cast<uint32_t>(r) * 128u;
+      // a bad page reads as zeros; V rows past the context are zero (their weights are
+      // 0, and 0 x NaN from unwritten slots must not reach P V)
+      if (sm.stage_bad[st] != 0 || (is_v && r >= nvalid)) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (c << 4), 0u, 0u, 0u, 0u);
+        if (is_v)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + kVHalfBytes + (c << 4), 0u, 0u, 0u, 0u);
+      } else {
+        const uint8_t* row = (is_v ? sm.vc[st] : sm.kc[st]) + r * 64;
+        const uint2 sc = *reinterpret_cast<const uint2*>((is_v ? sm.vsc[st] : sm.ksc[st]) + r * 8);
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(row + ((c ^ h) << 4));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int k = c ^ h;
+          const uint32_t s2 = ((k & 2) ? sc.y : sc.x) >> ((k & 1) * 16);
+          if (is_v)
+            dq_chunk_v(lut_t, v[c], s2, row_addr, r7, k);
+          else
+            dq_chunk(lut_t, v[c], s2, row_addr, r7, k);
+        }
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.tile_full[buf]));
+        mbar_arrive(smem_u32(&sm.raw_empty[st]));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================= MMA warp: S_j = Q K_j^T, then O += P_j V_j (S_{j+1} issued first)
+    if (lane == 0) {
+      const uint64_t qdesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
+      const uint32_t id_qk = idesc_e4m3_f32(128, kBlock, false, false);
+      const uint32_t id_pv = idesc_f16_f32(128, kDim / 2, true);
+      auto qk = [&](int j) -> bool {
+        const int bb = j % kTileBufs;
+        if (!wait_bar(smem_u32(&sm.tile_full[bb]), (j / kTileBufs) & 1, p.flags)) return false;
+        if (j >= kTileBufs && !wait_bar(smem_u32(&sm.s_free[bb]), ((j / kTileBufs) - 1) & 1, p.flags)) return false;
+        tc_fence_after();
+        // K step kk of an operand: +32 bytes along K-major rows (+2 in the address field)
+        const uint64_t kdesc = sdesc_kmajor_sw128(smem_u32(sm.ktile[bb]));
+#pragma unroll
+        for (int kk = 0; kk < kDim / 32; ++kk)
+          mma_f8_ss(tbase + kColS + kBlock * bb, qdesc + 2 * kk, kdesc + 2 * kk, id_qk, kk > 0);
+        mma_commit(smem_u32(&sm.s_full[bb]));
+        return true;
+      };
+      bool good = nmy == 0 || qk(0);
+      for (int j = 0; good && j < nmy; ++j) {
+        if (j + 1 < nmy && !qk(j + 1)) break;
+        const int bb = j % kTileBufs;
+        if (!wait_bar(smem_u32(&sm.p_full[bb]), (j / kTileBufs) & 1, p.flags)) break;
+        tc_fence_after();
+        // MN-major V halves (64 dims each = one 128-byte swizzle atom, 8-key groups 1 KB
+        // apart): K step kk = 16 keys = 2048 bytes (+128 in the field); A = P, 8 columns
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          const uint64_t vdesc = sdesc_kmajor_sw128(smem_u32(sm.vtile[bb][hv]));
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_f16_tmemA(tbase + kColO + 64 * hv, tbase + kColP + 64 * bb + 8 * kk, vdesc + 128 * kk, id_pv,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&sm.o_done));
+        mma_commit(smem_u32(&sm.tile_free[bb]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax warps: row m = TMEM lane; half hf = keys / dims 64 hf .. 64 hf + 63
+    const int hf = warp >> 2;
+    const int m = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int rq = m / kQPerKV;
+    const int pos_max = N - R + rq;  // this row sees key positions <= pos_max
+    const float c = p.sm_scale_log2;
+    float mrun = -INFINITY, lrun = 0.f;  // running max (log2 domain) and this half's running sum
+    bool good = true;
+    for (int j = 0; j < nmy; ++j) {
+      const int bb = j % kTileBufs;
+      const int pos0 = sm.ids[jb0 + j] * kBlock;
+      const bool full_vis = pos0 + kBlock - 1 <= N - R;  // every key visible to every row
+      const int lim = pos_max - pos0 - 64 * hf;           // key 64 hf + n visible iff n <= lim
+      if (good && !wait_bar(smem_u32(&sm.s_full[bb]), (j / kTileBufs) & 1, p.flags)) good = false;
+      good = __all_sync(0xFFFFFFFFu, good);  // warp-uniform from here (collective TMEM loads)
+      float sv[64];
+      float mx = -INFINITY;
+      if (good) {
+        tc_fence_after();
+        const uint32_t s_addr = tbase + lane_base + kColS + kBlock * bb + 64 * hf;
+        uint32_t v0[32], v1[32];
+        tmem_ld32(s_addr, v0);
+        tmem_ld32(s_addr + 32, v1);
+        tc_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          sv[u] = __uint_as_float(v0[u]);
+          sv[32 + u] = __uint_as_float(v1[u]);
+        }
+        if (!full_vis)
+#pragma unroll
+          for (int u = 0; u < 64; ++u) sv[u] = u <= lim ? sv[u] : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 64; u += 2) mx = fmaxf(mx, fmaxf(sv[u], sv[u + 1]));
+      }
+      // the other half's maximum of this row (scores are raw here: c > 0 keeps the order);
+      // the 4 softmax warps pass the same barriers every block, and give up together
+      sm.xmax[hf][m] = mx;
+      if (!good) sm.soft_dead = 1;
+      named_bar_sync(1, kSoftWarps * 32);
+      const float mo = sm.xmax[hf ^ 1][m];
+      const bool dead = sm.soft_dead != 0;
+      named_bar_sync(1, kSoftWarps * 32);  // both halves have read before the next block writes
+      if (dead) {
+        good = false;
+        break;
+      }
+      const float bmax = fmaxf(mx, mo) * c;
+      const float m_new = fmaxf(mrun, bmax);
+      const float ref = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(mrun - ref);  // 0 while nothing was seen yet
+      // the previous P V must be done before O is rescaled and this P buffer reused
+      if (j >= 1) {
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.o_done), (j - 1) & 1, p.flags))) {
+          good = false;  // leaves at the next block's barriers, with the other warps
+          continue;
+        }
+        tc_fence_after();
+        if (__any_sync(0xFFFFFFFFu, m_new > mrun && mrun != -INFINITY)) {
+          const float a = (m_new > mrun && mrun != -INFINITY) ? alpha : 1.f;
+#pragma unroll
+          for (int qc = 0; qc < 2; ++qc) {
+            uint32_t v[32];
+            const uint32_t o_addr = tbase + lane_base + kColO + 64 * hf + 32 * qc;
+            tmem_ld32(o_addr, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * a);
+            tmem_st32(o_addr, v);
+          }
+        }
+      }
+      // P = exp2(s c - max) for this half's 64 keys, FP16 pairs (2 keys per TMEM column)
+      uint32_t pw[32];
+      uint32_t hsum = 0u;  // f16x2 partial sums
+#pragma unroll
+      for (int u2 = 0; u2 < 32; ++u2) {
+        const float d0 = fmaf(sv[2 * u2], c, -ref), d1 = fmaf(sv[2 * u2 + 1], c, -ref);
+        uint32_t hx, hp;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(hx) : "f"(d1), "f"(d0));
+        asm("ex2.approx.f16x2 %0, %1;" : "=r"(hp) : "r"(hx));
+        asm("add.rn.f16x2 %0, %0, %1;" : "+r"(hsum) : "r"(hp));
+        pw[u2] = hp;
+      }
+      tmem_st32(tbase + lane_base + kColP + 64 * bb + 32 * hf, pw);
+      {
+        float2 f;
+        asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+            : "=f"(f.x), "=f"(f.y)
+            : "r"(hsum));
+        lrun = lrun * alpha + (f.x + f.y);
+      }
+      mrun = m_new;
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sm.s_free[bb]));
+        mbar_arrive(smem_u32(&sm.p_full[bb]));
+      }
+    }
+    // ---- output: O / l once the last P V has finished (l = both halves' sums)
+    sm.xmax[hf][m] = lrun;
+    named_bar_sync(1, kSoftWarps * 32);
+    const float lrow = lrun + sm.xmax[hf ^ 1][m];
+    if (__all_sync(0xFFFFFFFFu, good && nmy > 0 && wait_bar(smem_u32(&sm.o_done), (nmy - 1) & 1, p.flags))) {
+      tc_fence_after();
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      const float lse2 = lrow > 0.f ? mrun + log2f(lrow) : -INFINITY;
+      const int hh = m % kQPerKV;
+#pragma unroll
+      for (int qc = 0; qc < 2; ++qc) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_base + kColO + 64 * hf + 32 * qc, v);
+        tc_wait_ld();
+        const int d0 = 64 * hf + 32 * qc;
+        if (m < M) {
+          if (p.splits == 1) {
+            uint4* out = reinterpret_cast<uint4*>(
+                p.out + ((static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh) * kDim + d0);
+#pragma unroll
+            for (int u8 = 0; u8 < 4; ++u8)
+              out[u8] = make_uint4(
+                  bf16x2_bits(__uint_as_float(v[8 * u8]) * inv, __uint_as_float(v[8 * u8 + 1]) * inv),
+                  bf16x2_bits(__uint_as_float(v[8 * u8 + 2]) * inv, __uint_as_float(v[8 * u8 + 3]) * inv),
+                  bf16x2_bits(__uint_as_float(v[8 * u8 + 4]) * inv, __uint_as_float(v[8 * u8 + 5]) * inv),
+                  bf16x2_bits(__uint_as_float(v[8 * u8 + 6]) * inv, __uint_as_float(v[8 * u8 + 7]) * inv));
+          } else {
+            const long long base =
+                (static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m + m;
+            float4* po = reinterpret_cast<float4*>(p.part_o + base * kDim + d0);
+#pragma unroll
+            for (int u4 = 0; u4 < 8; ++u4)
+              po[u4] = make_float4(__uint_as_float(v[4 * u4]) * inv, __uint_as_float(v[4 * u4 + 1]) * inv,
+                                   __uint_as_float(v[4 * u4 + 2]) * inv, __uint_as_float(v[4 * u4 + 3]) * inv);
+          }
+        }
+      }
+      if (m < M && hf == 0) {
+        if (p.splits == 1) {
+          if (p.lse != nullptr)
+            p.lse[(static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh] = lse2 * 0.69314718055994531f;
+        } else {
+          p.part_lse2[(static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m + m] = lse2;
+        }
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
 
   if (p.splits == 1) return;
   // ---- last CTA of this (request, group) merges the splits' partials
@@ -501,7 +510,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   const int nsplit_used = (sm.nsel + p.blocks_per_split - 1) / p.blocks_per_split;
   const long long stride = static_cast<long long>(p.num_reqs) * kGroups * p.max_m;
   // 1. per query row: the splits' weights exp2(lse2_s - ref) / sum, and the row's lse
-  float* wgt = &sm.comb_o[0][0][0];  // [M][kTopK], the block buffers are free now
+  float* wgt = sm.wgt;  // [M][kTopK]
   for (int mrow = tid; mrow < M; mrow += kAttnThreads) {
     const long long base = static_cast<long long>(pair) * p.max_m + mrow;
     float l2[kTopK];
@@ -548,7 +557,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   }
 }
 
-size_t attn_smem_bytes() { return sizeof(AttnSmem) + 128; }
+size_t attn_smem_bytes() { return sizeof(AttnSmem) + 1024; }
 
 cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st) {
   const size_t smem = attn_smem_bytes();

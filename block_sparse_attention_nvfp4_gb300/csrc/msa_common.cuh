@@ -109,6 +109,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+__device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -146,6 +156,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 // v[0..31] <- 32 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
@@ -169,9 +194,10 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> F32, K-major A and B.
-__device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N, bool negate_b) {
-  return (1u << 4) | (negate_b ? (1u << 14) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+// Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> F32, K-major A; B K-major
+// (b_mn = false: B stored as N rows of K) or MN-major (b_mn = true: K rows of N).
+__device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N, bool negate_b, bool b_mn = false) {
+  return (1u << 4) | (negate_b ? (1u << 14) : 0u) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 // D[tmem] (+)= A[tmem] x B[smem]^T, issued by one thread.
@@ -190,6 +216,20 @@ __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(
           d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor, kind::f16: F16 x F16 -> F32, K-major A, B K- or MN-major.
+__device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N, bool b_mn) {
+  return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D[tmem] (+)= A[tmem] x B[smem], F16 operands (K = 16 per instruction).
+__device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -234,18 +274,23 @@ __device__ __forceinline__ uint32_t e4m3_to_h2_bcast(uint32_t sbyte) {
   asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "r"(sbyte));
   return (h & 0xFFFFu) | (h << 16);
 }
+// E4M3 images of the magnitudes of E2M1 codes 0..7 times the scale magnitude
+// (E4M3 byte s, sign ignored): .x = codes 0..3, .y = codes 4..7, byte k = code k
+// (the e2m1x2 conversions take code pairs).
+__device__ __forceinline__ uint2 lut_magnitudes(uint32_t s) {
+  const uint32_t sc = e4m3_to_h2_bcast(s & 0x7Fu);
+  return make_uint2(cvt_e2m1x2_scaled(0x10, sc) | (cvt_e2m1x2_scaled(0x32, sc) << 16),
+                    cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16));
+}
 // One entry per thread of the block; 256 entries.
 __device__ __forceinline__ void build_lut(LutEntry* lut) {
   for (int s = threadIdx.x; s < 256; s += blockDim.x) {
-    // magnitudes of E2M1 codes 0..7 (the e2m1x2 conversions take code pairs)
-    const uint32_t sc = e4m3_to_h2_bcast(static_cast<uint32_t>(s & 0x7F));
-    const uint32_t lo = cvt_e2m1x2_scaled(0x10, sc) | (cvt_e2m1x2_scaled(0x32, sc) << 16);
-    const uint32_t hi = cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16);
+    const uint2 m = lut_magnitudes(static_cast<uint32_t>(s));
     LutEntry e;
-    e.p0 = lo;
-    e.p1 = hi;
-    e.n0 = __byte_perm(hi, 0, 0x0123);
-    e.n1 = __byte_perm(lo, 0, 0x0123);
+    e.p0 = m.x;
+    e.p1 = m.y;
+    e.n0 = __byte_perm(m.y, 0, 0x0123);
+    e.n1 = __byte_perm(m.x, 0, 0x0123);
     lut[s] = e;
   }
 }
