@@ -65,6 +65,7 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S (2 x 128 FP32, one per key), O (128 FP32, one per dim), P (2 x 64,
 // 2 FP16 keys per column)
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr float kRescaleLog2 = 8.f;  // O is rescaled only when the max grows by more than 2^8
 static_assert(kColP + 64 * kTileBufs <= kTmemCols, "TMEM buffers exceed the allocation");
 static_assert(kDqWarps * 32 == 2 * kBlock, "one dequant thread per K row and per V row");
 
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     if (lane == 0) {
       const uint64_t qdesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
       const uint32_t id_qk = idesc_e4m3_f32(128, kBlock, false, false);
-      const uint32_t id_pv = idesc_f16_f32(128, kDim / 2, true);
+      const uint32_t id_pv = idesc_f16_f32(128, kDim, true);
       auto qk = [&](int j) -> bool {
         const int bb = j % kTileBufs;
         if (!wait_bar(smem_u32(&sm.tile_full[bb]), (j / kTileBufs) & 1, p.flags)) return false;
@@ -321,16 +322,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         const int bb = j % kTileBufs;
         if (!wait_bar(smem_u32(&sm.p_full[bb]), (j / kTileBufs) & 1, p.flags)) break;
         tc_fence_after();
-        // MN-major V halves (64 dims each = one 128-byte swizzle atom, 8-key groups 1 KB
-        // apart): K step kk = 16 keys = 2048 bytes (+128 in the field); A = P, 8 columns
+        // MN-major V: 128 dims = two 128-byte swizzle atoms (the two halves, kVHalfBytes
+        // apart: the leading-dimension offset), 8-key groups 1 KB apart (the stride
+        // offset); K step kk = 16 keys = 2048 bytes (+128 in the field); A = P, 8 columns
+        const uint64_t vdesc = sdesc_mn_sw128(smem_u32(sm.vtile[bb][0]), kVHalfBytes);
 #pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          const uint64_t vdesc = sdesc_kmajor_sw128(smem_u32(sm.vtile[bb][hv]));
-#pragma unroll
-          for (int kk = 0; kk < kBlock / 16; ++kk)
-            mma_f16_tmemA(tbase + kColO + 64 * hv, tbase + kColP + 64 * bb + 8 * kk, vdesc + 128 * kk, id_pv,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          mma_f16_tmemA(tbase + kColO, tbase + kColP + 64 * bb + 8 * kk, vdesc + 128 * kk, id_pv,
+                        (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sm.o_done));
         mma_commit(smem_u32(&sm.tile_free[bb]));
       }
@@ -344,7 +343,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     const int rq = m / kQPerKV;
     const int pos_max = N - R + rq;  // this row sees key positions <= pos_max
     const float c = p.sm_scale_log2;
-    float mrun = -INFINITY, lrun = 0.f;  // running max (log2 domain) and this half's running sum
+    float mref = -INFINITY, lrun = 0.f;  // reference max (log2 domain) and this half's running sum
     bool good = true;
     for (int j = 0; j < nmy; ++j) {
       const int bb = j % kTileBufs;
@@ -385,30 +384,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         good = false;
         break;
       }
+      // Lazy rescale: P is taken relative to a reference max mref that moves only
+      // when this block's max exceeds it by more than kRescaleLog2 (P then stays
+      // below 2^kRescaleLog2, well inside FP16); O / l is exact whatever mref is.
       const float bmax = fmaxf(mx, mo) * c;
-      const float m_new = fmaxf(mrun, bmax);
+      const bool move = bmax > mref + kRescaleLog2 || (mref == -INFINITY && bmax != -INFINITY);
+      const float m_new = move ? bmax : mref;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = exp2f(mrun - ref);  // 0 while nothing was seen yet
-      // the previous P V must be done before O is rescaled and this P buffer reused
-      if (j >= 1) {
+      const float alpha = exp2f(mref - ref);  // 0 while nothing was seen yet
+      const bool rescale = move && mref != -INFINITY;
+      if (j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
+        // O must hold every earlier block before it is rescaled
         if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.o_done), (j - 1) & 1, p.flags))) {
           good = false;  // leaves at the next block's barriers, with the other warps
           continue;
         }
         tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, m_new > mrun && mrun != -INFINITY)) {
-          const float a = (m_new > mrun && mrun != -INFINITY) ? alpha : 1.f;
+        const float a = rescale ? alpha : 1.f;
 #pragma unroll
-          for (int qc = 0; qc < 2; ++qc) {
-            uint32_t v[32];
-            const uint32_t o_addr = tbase + lane_base + kColO + 64 * hf + 32 * qc;
-            tmem_ld32(o_addr, v);
-            tc_wait_ld();
+        for (int qc = 0; qc < 2; ++qc) {
+          uint32_t v[32];
+          const uint32_t o_addr = tbase + lane_base + kColO + 64 * hf + 32 * qc;
+          tmem_ld32(o_addr, v);
+          tc_wait_ld();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * a);
-            tmem_st32(o_addr, v);
-          }
+          for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * a);
+          tmem_st32(o_addr, v);
         }
+      } else if (j >= kTileBufs) {
+        // this P buffer's previous P V (block j - 2) must have finished reading it
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.tile_free[bb]), ((j / kTileBufs) - 1) & 1, p.flags))) {
+          good = false;
+          continue;
+        }
+        tc_fence_after();
       }
       // P = exp2(s c - max) for this half's 64 keys, FP16 pairs (2 keys per TMEM column)
       uint32_t pw[32];
@@ -430,7 +439,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
             : "r"(hsum));
         lrun = lrun * alpha + (f.x + f.y);
       }
-      mrun = m_new;
+      mref = m_new;
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -446,7 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     if (__all_sync(0xFFFFFFFFu, good && nmy > 0 && wait_bar(smem_u32(&sm.o_done), (nmy - 1) & 1, p.flags))) {
       tc_fence_after();
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-      const float lse2 = lrow > 0.f ? mrun + log2f(lrow) : -INFINITY;
+      const float lse2 = lrow > 0.f ? mref + log2f(lrow) : -INFINITY;
       const int hh = m % kQPerKV;
 #pragma unroll
       for (int qc = 0; qc < 2; ++qc) {

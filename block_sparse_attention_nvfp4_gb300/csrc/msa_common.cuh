@@ -194,6 +194,19 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(2u) << 61;                 // 128-byte swizzle
   return d;
 }
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle. Each K row
+// holds 128 bytes of the MN dimension (one swizzle atom); further atoms along MN
+// are `mn_atom_bytes` apart (leading byte offset), 8-row K groups 1024 bytes
+// apart (stride byte offset).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_atom_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((mn_atom_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
 // Instruction descriptor, kind::f8f6f4: E4M3 x E4M3 -> F32, K-major A; B K-major
 // (b_mn = false: B stored as N rows of K) or MN-major (b_mn = true: K rows of N).
 __device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N, bool negate_b, bool b_mn = false) {
