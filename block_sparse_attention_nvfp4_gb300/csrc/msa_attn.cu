@@ -54,8 +54,9 @@ constexpr int kMmaWarp = 2;                         // MMA issue, TMEM allocatio
 constexpr int kLoadWarp = 3;                        // raw page copies
 constexpr int kDqWarp0 = 6, kDqWarps = 8;           // warps 6..13: K rows (0..127), V rows (128..255)
 constexpr int kAttnThreads = (kDqWarp0 + kDqWarps) * 32;
-constexpr int kAttnStages = 4;                      // raw NVFP4 page ring
-constexpr int kTileBufs = 2;                        // dequantised K / V tiles, TMEM score and P buffers
+constexpr int kAttnStages = 2;                      // raw NVFP4 page ring
+constexpr int kTileBufs = 3;                        // dequantised K / V tiles
+constexpr int kSBufs = 2;                           // TMEM score and P buffers
 constexpr uint32_t kHeadPageBytes = kBlock * 64;    // codes of one (page, KV head)
 constexpr uint32_t kHeadScaleBytes = kBlock * 8;
 constexpr uint32_t kTileBytes = kBlock * kDim;      // one dequantised K tile (E4M3, 128-byte rows)
@@ -66,7 +67,7 @@ constexpr uint32_t kTmemCols = 512;
 // 2 FP16 keys per column)
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr float kRescaleLog2 = 8.f;  // O is rescaled only when the max grows by more than 2^8
-static_assert(kColP + 64 * kTileBufs <= kTmemCols, "TMEM buffers exceed the allocation");
+static_assert(kColP + 64 * kSBufs <= kTmemCols, "TMEM buffers exceed the allocation");
 static_assert(kDqWarps * 32 == 2 * kBlock, "one dequant thread per K row and per V row");
 
 struct AttnSmem {
@@ -83,7 +84,7 @@ struct AttnSmem {
   int soft_dead;                                    // a softmax warp gave up waiting
   uint64_t raw_full[kAttnStages], raw_empty[kAttnStages];
   uint64_t tile_full[kTileBufs], tile_free[kTileBufs];
-  uint64_t s_full[kTileBufs], s_free[kTileBufs], p_full[kTileBufs], o_done;
+  uint64_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs], p_free[kSBufs], o_done;
   int stage_bad[kAttnStages];
   int ids[kTopK];
   int phys[kTopK];                                  // block-table entries of the selected blocks
@@ -165,9 +166,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     for (int t = 0; t < kTileBufs; ++t) {
       mbar_init(smem_u32(&sm.tile_full[t]), kDqWarps);
       mbar_init(smem_u32(&sm.tile_free[t]), 1);
+    }
+    for (int t = 0; t < kSBufs; ++t) {
       mbar_init(smem_u32(&sm.s_full[t]), 1);
       mbar_init(smem_u32(&sm.s_free[t]), kSoftWarps);
       mbar_init(smem_u32(&sm.p_full[t]), kSoftWarps);
+      mbar_init(smem_u32(&sm.p_free[t]), 1);
     }
     mbar_init(smem_u32(&sm.o_done), 1);
     mbar_fence_init();
@@ -298,40 +302,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       }
     }
   } else if (warp == kMmaWarp) {
-    // ================= MMA warp: S_j = Q K_j^T, then O += P_j V_j (S_{j+1} issued first)
+    // ================= MMA warp: S_j = Q K_j^T and O += P_j V_j, each issued as soon as
+    // its inputs are ready (S_{j+1} does not wait behind P_j V_j or the reverse)
     if (lane == 0) {
       const uint64_t qdesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
       const uint32_t id_qk = idesc_e4m3_f32(128, kBlock, false, false);
       const uint32_t id_pv = idesc_f16_f32(128, kDim, true);
-      auto qk = [&](int j) -> bool {
-        const int bb = j % kTileBufs;
-        if (!wait_bar(smem_u32(&sm.tile_full[bb]), (j / kTileBufs) & 1, p.flags)) return false;
-        if (j >= kTileBufs && !wait_bar(smem_u32(&sm.s_free[bb]), ((j / kTileBufs) - 1) & 1, p.flags)) return false;
-        tc_fence_after();
-        // K step kk of an operand: +32 bytes along K-major rows (+2 in the address field)
-        const uint64_t kdesc = sdesc_kmajor_sw128(smem_u32(sm.ktile[bb]));
+      int nq = 0, np = 0;  // next block for S, next block for P V
+      long long t_last = global_ns();
+      while (np < nmy) {
+        bool did = false;
+        if (nq < nmy) {
+          const int tb = nq % kTileBufs, sb = nq % kSBufs;
+          if (mbar_test(smem_u32(&sm.tile_full[tb]), (nq / kTileBufs) & 1) &&
+              (nq < kSBufs || mbar_test(smem_u32(&sm.s_free[sb]), ((nq / kSBufs) - 1) & 1))) {
+            tc_fence_after();
+            // K step kk of an operand: +32 bytes along K-major rows (+2 in the address field)
+            const uint64_t kdesc = sdesc_kmajor_sw128(smem_u32(sm.ktile[tb]));
 #pragma unroll
-        for (int kk = 0; kk < kDim / 32; ++kk)
-          mma_f8_ss(tbase + kColS + kBlock * bb, qdesc + 2 * kk, kdesc + 2 * kk, id_qk, kk > 0);
-        mma_commit(smem_u32(&sm.s_full[bb]));
-        return true;
-      };
-      bool good = nmy == 0 || qk(0);
-      for (int j = 0; good && j < nmy; ++j) {
-        if (j + 1 < nmy && !qk(j + 1)) break;
-        const int bb = j % kTileBufs;
-        if (!wait_bar(smem_u32(&sm.p_full[bb]), (j / kTileBufs) & 1, p.flags)) break;
-        tc_fence_after();
-        // MN-major V: 128 dims = two 128-byte swizzle atoms (the two halves, kVHalfBytes
-        // apart: the leading-dimension offset), 8-key groups 1 KB apart (the stride
-        // offset); K step kk = 16 keys = 2048 bytes (+128 in the field); A = P, 8 columns
-        const uint64_t vdesc = sdesc_mn_sw128(smem_u32(sm.vtile[bb][0]), kVHalfBytes);
+            for (int kk = 0; kk < kDim / 32; ++kk)
+              mma_f8_ss(tbase + kColS + kBlock * sb, qdesc + 2 * kk, kdesc + 2 * kk, id_qk, kk > 0);
+            mma_commit(smem_u32(&sm.s_full[sb]));
+            ++nq;
+            did = true;
+          }
+        }
+        if (np < nq) {
+          const int tb = np % kTileBufs, sb = np % kSBufs;
+          if (mbar_test(smem_u32(&sm.p_full[sb]), (np / kSBufs) & 1)) {
+            tc_fence_after();
+            // MN-major V: 128 dims = two 128-byte swizzle atoms (the two halves, kVHalfBytes
+            // apart: the leading-dimension offset), 8-key groups 1 KB apart (the stride
+            // offset); K step kk = 16 keys = 2048 bytes (+128 in the field); A = P, 8 columns
+            const uint64_t vdesc = sdesc_mn_sw128(smem_u32(sm.vtile[tb][0]), kVHalfBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_f16_tmemA(tbase + kColO, tbase + kColP + 64 * bb + 8 * kk, vdesc + 128 * kk, id_pv,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&sm.o_done));
-        mma_commit(smem_u32(&sm.tile_free[bb]));
+            for (int kk = 0; kk < kBlock / 16; ++kk)
+              mma_f16_tmemA(tbase + kColO, tbase + kColP + 64 * sb + 8 * kk, vdesc + 128 * kk, id_pv,
+                            (np > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&sm.o_done));
+            mma_commit(smem_u32(&sm.tile_free[tb]));
+            mma_commit(smem_u32(&sm.p_free[sb]));
+            ++np;
+            did = true;
+          }
+        }
+        const long long now = global_ns();
+        if (did) {
+          t_last = now;
+        } else if (now - t_last > kWaitLimitNs) {
+          set_flag(p.flags, kFlagTimeout);
+          break;
+        }
       }
     }
     __syncwarp();
@@ -346,11 +367,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     float mref = -INFINITY, lrun = 0.f;  // reference max (log2 domain) and this half's running sum
     bool good = true;
     for (int j = 0; j < nmy; ++j) {
-      const int bb = j % kTileBufs;
+      const int bb = j % kSBufs;
       const int pos0 = sm.ids[jb0 + j] * kBlock;
       const bool full_vis = pos0 + kBlock - 1 <= N - R;  // every key visible to every row
       const int lim = pos_max - pos0 - 64 * hf;           // key 64 hf + n visible iff n <= lim
-      if (good && !wait_bar(smem_u32(&sm.s_full[bb]), (j / kTileBufs) & 1, p.flags)) good = false;
+      if (good && !wait_bar(smem_u32(&sm.s_full[bb]), (j / kSBufs) & 1, p.flags)) good = false;
       good = __all_sync(0xFFFFFFFFu, good);  // warp-uniform from here (collective TMEM loads)
       float sv[64];
       float mx = -INFINITY;
@@ -411,9 +432,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
           for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * a);
           tmem_st32(o_addr, v);
         }
-      } else if (j >= kTileBufs) {
+      } else if (j >= kSBufs) {
         // this P buffer's previous P V (block j - 2) must have finished reading it
-        if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.tile_free[bb]), ((j / kTileBufs) - 1) & 1, p.flags))) {
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.p_free[bb]), ((j / kSBufs) - 1) & 1, p.flags))) {
           good = false;
           continue;
         }

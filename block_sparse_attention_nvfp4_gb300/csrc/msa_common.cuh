@@ -70,6 +70,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test: has phase `parity` of `bar` completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for phase `parity` of `bar` to complete, for at most kWaitLimitNs.
 // On timeout sets the timeout flag and returns false.
 static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* flags) {
