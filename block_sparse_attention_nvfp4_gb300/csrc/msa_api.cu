@@ -292,7 +292,9 @@ static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids
   SelectParams p = select_params(args, w, ids, scores_out);
   p.token_scores = tok;
   p.score_stride = stride;
-  return launch_select(map, p, mode, d.sm_count, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  if (launch_select(map, p, mode, d.sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (mode == 0 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
+  return MSA_OK;
 }
 
 msa_status msa_index_scores(const msa_decode_args* args, float* scores, int64_t score_stride, void* ws,

@@ -444,6 +444,8 @@ static __device__ __noinline__ void topk_by_insertion(const float* S, int nc, in
 }
 
 // scratch: 64 u64 per warp (shared memory), for the threshold filter's survivors.
+// S may be global or shared memory (callers stage large score rows in shared
+// memory, where the passes below do not wait on dependent global round trips).
 static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* ids_out, uint64_t* scratch) {
   const int lane = threadIdx.x & 31;
   if (nb <= kTopK) {
@@ -454,8 +456,9 @@ static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* i
   const int nc = nb - 1;  // candidates: every block but the recent one
   int32_t* sel = reinterpret_cast<int32_t*>(scratch + 48);  // 15 winners (kept apart from survivors 0..47)
   // 1. each lane's best key; loads issued 8 at a time (4 blocks per 16-byte load)
+  constexpr int kBatch = 32 * 4 * 8;
   uint64_t lmax = 0ull;
-  for (int base = 0; base < nc; base += 32 * 4 * 8) {
+  for (int base = 0; base < nc; base += kBatch) {
     float4 v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -477,26 +480,39 @@ static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* i
   // 2. the 15th largest lane maximum bounds the answer: the 15 largest lane maxima
   //    are 15 distinct candidates, so the 15th best candidate is at least that large
   const uint64_t T = shfl_u64(warp_sort_desc(lmax), L - 1);
-  // 3. survivors: every candidate with key >= T (contains the exact top 15)
+  // 3. survivors: every candidate with key >= T (contains the exact top 15); the scores
+  //    are read again 8 loads at a time (one round trip per 1,024 candidates)
   int count = 0;
-  for (int base = 0; base < nc; base += 32 * 4) {
-    const int c = base + lane * 4;
-    float4 v = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float e[4] = {v.x, v.y, v.z, v.w};
+  for (int base = 0; base < nc; base += kBatch) {
+    float4 v[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool keep = c + q < nc && topk_key(e[q], c + q) >= T;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-      if (keep) {
+    for (int u = 0; u < 8; ++u) {
+      const int c = base + (u * 32 + lane) * 4;
+      v[u] = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = base + (u * 32 + lane) * 4;
+      const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t key = topk_key(e[q], c + q);
+        const bool keep = c + q < nc && key >= T;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
         const int pos = count + __popc(bal & ((1u << lane) - 1u));
-        if (pos < 48) scratch[pos] = topk_key(e[q], c + q);
+        if (keep && pos < 48) scratch[pos] = key;  // predicated, no divergent branch
+        count += __popc(bal);
       }
-      count += __popc(bal);
     }
   }
   __syncwarp();
   if (count > 48) {
     topk_by_insertion(S, nc, sel);
+  } else if (count <= 32) {
+    // 4. the survivors, one per lane, sorted descending: the top 15 are lanes 0..14
+    const uint64_t k = warp_sort_desc(lane < count ? scratch[lane] : 0ull);
+    if (lane < L) sel[lane] = topk_id(k);
+    __syncwarp();
   } else {
     // 4. exact rank among the survivors
     for (int i = lane; i < count; i += 32) {

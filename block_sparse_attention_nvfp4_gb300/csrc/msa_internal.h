@@ -18,7 +18,7 @@ struct SelectParams {
   const uint8_t* ki_scale;
   float* block_S;           // workspace [B][4][s_stride] block scores
   int s_stride;             // max_pages rounded up to a multiple of 4 (16-byte rows)
-  uint32_t* req_cnt;        // workspace [B] arrival counters
+  uint32_t* req_cnt;        // workspace [B] (unused by the kernels; kept in the layout)
   uint32_t* flags;          // workspace error flags
   int32_t* block_ids;       // [B][4][16]
   float* block_scores_out;  // optional [B][4][max_pages]
@@ -82,6 +82,9 @@ size_t attn_smem_bytes();
 // grid: a fixed number of CTAs per SM over `sm_count` SMs
 cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,
                           cudaStream_t st);
+// top-k of the block scores the scan (mode 0) wrote: one CTA per request, chained
+// to the scan with programmatic dependent launch
+cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st);
 cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
 cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,

@@ -138,5 +138,6 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
   p.s_stride = score_stride(args->max_pages_per_req);
   p.block_ids = block_ids;
   p.block_scores_out = block_scores;
-  return launch_select(map, p, 0, sms, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  if (launch_select(map, p, 0, sms, st) != cudaSuccess) return MSA_ERR_CUDA;
+  return launch_topk(p, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

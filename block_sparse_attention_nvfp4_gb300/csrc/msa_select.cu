@@ -37,6 +37,7 @@
 // completes a request's block scores (an arrival counter, no waiting) runs the
 // top-k for that request: one warp per group.
 #include <climits>
+#include <cstddef>
 
 #include "msa_common.cuh"
 #include "msa_internal.h"
@@ -60,26 +61,31 @@ constexpr uint32_t kScaleBytes = kBlock * 8;    // its scales
 constexpr uint32_t kTileBytes = kBlock * kDim;  // one dequantised page (E4M3)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kDCols = kBlock;             // D buffer: 128 FP32 columns (tokens)
-constexpr int kCtaPages = 2048;                 // block-table entries staged per CTA
+constexpr int kCtaPages = 1024;                 // block-table entries staged per CTA
+constexpr int kLutCopies = 16;                  // one per thread of a 16-thread (8-byte) wavefront
 static_assert(kDBufs * kDCols <= kTmemCols, "TMEM buffers exceed the allocation");
 
 struct Smem {
   // A operand: rows 0..31 hold the request's index queries. The MMA reads a
-  // 128-row tile, so rows 32..127 are the next 12 KB (the table and the staged
-  // block table, written once before the first MMA); their D lanes are never read.
+  // 128-row tile, so rows 32..127 are the next 12 KB (the table, written once
+  // before the first MMA); their D lanes are never read.
   uint8_t qtile[32 * 128];                  // offset 0
-  LutEntry lut[256];                        // 4 KB
-  int32_t phys[kCtaPages];                  // 8 KB: this CTA's block-table entries (when its range fits)
+  // scaled magnitudes per scale magnitude, 16 interleaved copies (entry e of copy c
+  // at 8 (16 e + c) bytes): the 16 threads of an 8-byte wavefront read 16
+  // different banks whatever their scales
+  uint2 lut[128 * kLutCopies];              // 16 KB
+  int32_t phys[kCtaPages];                  // 4 KB: this CTA's block-table entries (when its range fits)
   uint8_t codes[kStages][kCodeBytes];       // offset 16 KB, 1024-aligned
   uint8_t tile[kBBufs][kTileBytes];         // B operand (SW128), 1024-aligned
   uint8_t scales[kStages][kScaleBytes];
   uint64_t full[kStages], empty[kStages];
   uint64_t bfull[kBBufs], bfree[kBBufs], dfull[kDBufs], dempty[kDBufs];
   uint32_t taddr;
-  int ntodo;
+  uint32_t fma_k[4];                        // 65536, 16: constants the compiler cannot fold
 };
-static_assert(sizeof(LutEntry) * 256 + sizeof(int32_t) * kCtaPages == 96 * 128,
-              "rows 32..127 of the A tile must cover the table and the staged block table exactly");
+static_assert(sizeof(uint2) * 128 * kLutCopies >= 96 * 128, "rows 32..127 of the A tile lie in the table");
+static_assert(offsetof(Smem, codes) % 1024 == 0 && offsetof(Smem, tile) % 1024 == 0, "swizzled tiles");
+static_assert(offsetof(Smem, scales) % 16 == 0, "bulk copies need 16-byte alignment");
 
 struct PageCursor {
   int b;       // request
@@ -139,17 +145,35 @@ __device__ __forceinline__ float max32_masked(const uint32_t (&v)[32], int n0, i
   return m;
 }
 
+// Signed dequantisation of one code word (8 elements) to two words of E4M3 bytes,
+// as dq8_signed, with its two shifts on the multiply-add pipe (k16 = 65536 and
+// k4 = 16 come from shared memory, so the compiler cannot turn them back into
+// shifts): the byte permutes and logic already fill the integer pipe.
+__device__ __forceinline__ void dq8_signed_fma(uint32_t w, uint32_t L0, uint32_t L1, uint32_t k16, uint32_t k4,
+                                               uint32_t& r0, uint32_t& r1) {
+  const uint32_t sel = w & 0x77777777u;
+  const uint32_t m0 = prmt(L0, L1, sel);
+  const uint32_t m1 = prmt(L0, L1, __umulhi(sel, k16));  // sel >> 16
+  const uint32_t u = w * k4;                              // w << 4
+  const uint32_t s0 = prmt(w, u, 0x1504);  // byte k's msb = sign of nibble k, k = 0..3
+  const uint32_t s1 = prmt(w, u, 0x3726);  // nibbles 4..7
+  r0 = m0 ^ (s0 & 0x80808080u);
+  r1 = m1 ^ (s1 & 0x80808080u);
+}
+
 // Dequantise 8 code words (4 groups of 16 elements; scale byte q of scw belongs to
 // words 2q, 2q+1) to 64 signed E4M3 bytes and store them as 16-byte chunks
 // c0..c0+3 of a K-major SW128 row (chunk c of row r sits at chunk c ^ (r & 7)).
-__device__ __forceinline__ void dequant_half_to_tile(const LutEntry* lut, const uint32_t* w, uint32_t scw,
-                                                     uint32_t row_addr, int r7, int c0) {
+// lut_t: this thread's copy of the table (entry e at lut_t + 128 e).
+__device__ __forceinline__ void dequant_half_to_tile(uint32_t lut_t, const uint32_t* w, uint32_t scw, uint32_t k16,
+                                                     uint32_t k4, uint32_t row_addr, int r7, int c0) {
   uint32_t out[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const LutEntry L = lut[(scw >> (8 * q)) & 0xFFu];
+    const uint2 L = lds_u2(lut_t + (((scw >> (8 * q)) & 0x7Fu) << 7));
 #pragma unroll
-    for (int h = 0; h < 2; ++h) dq8_signed(w[2 * q + h], L.p0, L.p1, out[4 * q + 2 * h], out[4 * q + 2 * h + 1]);
+    for (int h = 0; h < 2; ++h)
+      dq8_signed_fma(w[2 * q + h], L.x, L.y, k16, k4, out[4 * q + 2 * h], out[4 * q + 2 * h + 1]);
   }
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc)
@@ -185,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   int* rows_s = nb + (p.num_reqs + 1);                                     // [B]
   int* row0_s = rows_s + p.num_reqs;                                        // [B]
   int* ctx_s = row0_s + p.num_reqs;                                         // [B]
-  int* todo = ctx_s + p.num_reqs;                                           // [B]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.num_reqs;
@@ -229,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       acc += nb[b];
     }
     if (lane == 31) prefix[B] = incl;
-    if (lane == 0) sm.ntodo = 0;
   }
   __syncthreads();
   const long long total = prefix[B];
@@ -237,23 +259,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const long long p0 = total * blockIdx.x / G, p1 = total * (blockIdx.x + 1) / G;
   const int n = static_cast<int>(p1 - p0);
 
-  // requests with no pages get empty selections (written by CTA 0)
-  if (MODE == 0 && blockIdx.x == 0) {
-    for (int i = tid; i < B * kGroups * kTopK; i += kThreads) {
-      const int b = i / (kGroups * kTopK);
-      if (nb[b] == 0) p.block_ids[i] = -1;
-    }
-    if (p.block_scores_out != nullptr)
-      for (long long i = tid; i < static_cast<long long>(B) * kGroups * p.max_pages; i += kThreads) {
-        const int b = static_cast<int>(i / (kGroups * p.max_pages));
-        if (nb[b] == 0) p.block_scores_out[i] = -INFINITY;
-      }
-  }
   if (n <= 0) return;
 
   // ---- setup: table, barriers, tensor memory
-  build_lut(sm.lut);
+  for (int u = tid; u < 128 * kLutCopies; u += kThreads) sm.lut[u] = lut_magnitudes(static_cast<uint32_t>(u / kLutCopies));
   if (tid == 0) {
+    sm.fma_k[0] = 65536u;
+    sm.fma_k[1] = 16u;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 4);  // the 4 warps of the page's dequant group
@@ -372,6 +384,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int r7 = r & 7, sw = (r >> 1) & 3;
     const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + static_cast<uint32_t>(r7) * 128u;
     const uint32_t tile0 = smem_u32(sm.tile[0]);
+    const uint32_t lut_t = smem_u32(sm.lut) + static_cast<uint32_t>(lane % kLutCopies) * 8u;
+    const uint32_t k16 = sm.fma_k[0], k4 = sm.fma_k[1];
     for (int i = grp; i < n; i += kDqGroups) {
       const int s = i % kStages, j = i % kBBufs;
       uint32_t w[16];
@@ -396,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tc_fence_after();
       }
       const uint32_t row_addr = tile0 + j * kTileBytes + row_off;
-      dequant_half_to_tile(sm.lut, w, sc.x, row_addr, r7, 0);
-      dequant_half_to_tile(sm.lut, w + 8, sc.y, row_addr, r7, 4);
+      dequant_half_to_tile(lut_t, w, sc.x, k16, k4, row_addr, r7, 0);
+      dequant_half_to_tile(lut_t, w + 8, sc.y, k16, k4, row_addr, r7, 4);
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.bfull[j]));
@@ -463,42 +477,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
-  if (MODE != 0 || !all_alive) return;
+  (void)all_alive;
+}
 
-  // ---- arrival: the CTA completing a request's block scores runs its top-k
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    PageCursor pc = cursor_at(p0, prefix, B);
-    long long q = p0;
-    while (q < p1) {
-      const int b = pc.b;
-      const long long end = prefix[b + 1] < p1 ? prefix[b + 1] : p1;
-      const unsigned cnt = static_cast<unsigned>(end - q);
-      const unsigned old = atomicAdd(p.req_cnt + b, cnt);
-      if (old + cnt == static_cast<unsigned>(nb[b])) {
-        p.req_cnt[b] = 0u;
-        todo[sm.ntodo++] = b;
-      }
-      q = end;
-      pc.b = b + 1;
-      pc.c = 0;
-      while (pc.b < B && nb[pc.b] == 0) ++pc.b;
-    }
+// Step 3 of the fused selection, after the scan: one CTA per request, warp g takes
+// group g's block scores (staged in shared memory when the row fits), the top 15
+// plus the most recent block. A kernel of its own so it runs on SMs the scan has
+// left (measured on GB300: run by the scan's last CTA per request, beside a CTA
+// still scanning, it took about 15 us; here it runs on idle SMs).
+__global__ void __launch_bounds__(128) topk_kernel(const SelectParams p, int stage_row) {
+  extern __shared__ float tk_stage[];  // [4][stage_row] block scores (stage_row = 0: read global)
+  __shared__ uint64_t scratch[kGroups][64];
+  pdl_launch_dependents();
+  pdl_wait_primary();  // the block scores come from the scan kernel
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.context_lens[b];
+  const int r0 = p.q_indptr[b], R = p.q_indptr[b + 1] - r0;
+  const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
+                  r0 + R <= p.total_rows;
+  const int nbb = ok && R > 0 ? (N + kBlock - 1) / kBlock : 0;
+  int32_t* ids = p.block_ids + (static_cast<long long>(b) * kGroups + warp) * kTopK;
+  if (nbb == 0) {  // no pages: an empty selection
+    if (lane < kTopK) ids[lane] = -1;
+    if (p.block_scores_out != nullptr)
+      for (int c = lane; c < p.max_pages; c += 32)
+        p.block_scores_out[(static_cast<long long>(b) * kGroups + warp) * p.max_pages + c] = -INFINITY;
+    return;
   }
-  __syncthreads();
-  __threadfence();
-  uint64_t* tk_scratch = reinterpret_cast<uint64_t*>(sm.codes[0]) + 64 * warp;  // stages are free now
-  for (int k = 0; k < sm.ntodo; ++k) {
-    const int b = todo[k];
-    if (warp < kGroups) {
-      const float* S = p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
-      warp_topk(S, nb[b], p.block_ids + (static_cast<long long>(b) * kGroups + warp) * kTopK, tk_scratch);
-      if (p.block_scores_out != nullptr) {
-        float* o = p.block_scores_out + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
-        for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nb[b] ? S[c] : -INFINITY;
-      }
+  const bool staged = stage_row >= nbb;
+  if (staged) {
+    const int row4 = (nbb + 3) / 4;  // float4 per group row (block_S rows are 16-byte padded)
+    for (int u = threadIdx.x; u < kGroups * row4; u += blockDim.x) {
+      const int g = u / row4, c4 = u - g * row4;
+      reinterpret_cast<float4*>(tk_stage + g * stage_row)[c4] = __ldcg(
+          reinterpret_cast<const float4*>(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride) + c4);
     }
+    __syncthreads();
+  }
+  const float* S = staged ? tk_stage + warp * stage_row
+                          : p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
+  warp_topk(S, nbb, ids, scratch[warp]);
+  if (p.block_scores_out != nullptr) {
+    float* o = p.block_scores_out + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
+    for (int c = lane; c < p.max_pages; c += 32) o[c] = c < nbb ? S[c] : -INFINITY;
   }
 }
 
@@ -581,7 +602,7 @@ __global__ void dequant_rows_kernel(const uint8_t* codes, const uint8_t* scales,
 
 size_t select_smem_bytes(int num_reqs) {
   const size_t need = sizeof(Smem) + sizeof(long long) * (num_reqs + 1) + sizeof(int) * (num_reqs + 1) +
-                      4 * sizeof(int) * num_reqs + 1024;
+                      3 * sizeof(int) * num_reqs + 1024;
   // at least 80 KB so no more than two CTAs share an SM's 512 tensor-memory columns
   return need > 80 * 1024 ? need : 80 * 1024;
 }
@@ -600,6 +621,27 @@ cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, in
     if (e != cudaSuccess) return e;
     select_kernel<1><<<grid, kThreads, smem, st>>>(ki_map, prm);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st) {
+  // stage each group's score row in shared memory when the 4 rows fit in 160 KB
+  const int stage_row = static_cast<size_t>(kGroups) * prm.s_stride * sizeof(float) <= 160 * 1024 ? prm.s_stride : 0;
+  const size_t smem = static_cast<size_t>(kGroups) * stage_row * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.num_reqs, 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_kernel, prm, stage_row);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
