@@ -46,14 +46,18 @@ namespace msa {
 
 namespace {
 
-// Warp roles. TMEM lanes 0..31 (the D rows read back) belong to warps with
-// warp % 4 == 0, so the two epilogue warps are 0 and 4 (page i -> warp 4 * (i % 2)).
-constexpr int kLoadWarp = 1;   // TMA producer
-constexpr int kIssueWarp = 2;  // MMA issue, query tile, TMEM allocation
+// Warp roles. Warp w runs on SM sub-partition w % 4 and reads TMEM lanes
+// 32 (w % 4) .. + 31. D buffer e holds the 32 query columns in lanes 32e .. 32e + 31
+// (its A tile starts 32 rows earlier for e = 1), so epilogue warps 0 and 1 read
+// buffers 0 and 1 (pages i with i % 2 = e), and every sub-partition runs one warp of
+// each dequant group plus one of: epilogue, epilogue, load, MMA (measured on GB300:
+// with 3 of the 8 dequant warps on one sub-partition, those lagged the group).
+constexpr int kLoadWarp = 2;   // TMA producer
+constexpr int kIssueWarp = 3;  // MMA issue, query tile, TMEM allocation
+constexpr int kDqWarp0 = 4;    // dequant warps 4..11: group (w - 4) / 4, one warp per sub-partition
 constexpr int kDqGroups = 2;   // page i is dequantised by group i % kDqGroups
-constexpr int kDqWarps = 4 * kDqGroups;  // warps 3, 5..11; 4 warps (128 tokens) per group
-constexpr int kThreads = 12 * 32;
-static_assert(kThreads == (4 + kDqWarps) * 32, "2 epilogue + load + MMA + dequant warps");
+constexpr int kDqWarps = 4 * kDqGroups;
+constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kCtasPerSm = 2;
 constexpr int kStages = 4, kBBufs = 3, kDBufs = 2;
 constexpr uint32_t kCodeBytes = kBlock * 64;    // one page of index-key codes
@@ -66,15 +70,16 @@ constexpr int kLutCopies = 16;                  // one per thread of a 16-thread
 static_assert(kDBufs * kDCols <= kTmemCols, "TMEM buffers exceed the allocation");
 
 struct Smem {
-  // A operand: rows 0..31 hold the request's index queries. The MMA reads a
-  // 128-row tile, so rows 32..127 are the next 12 KB (the table, written once
-  // before the first MMA); their D lanes are never read.
-  uint8_t qtile[32 * 128];                  // offset 0
+  int32_t phys[kCtaPages];                  // offset 0, 4 KB: this CTA's block-table entries (when they fit)
+  // A operand: the request's index queries, 32 rows of 128 bytes. The MMA reads a
+  // 128-row tile starting at qtile (D buffer 0: queries in rows 0..31) or 32 rows
+  // before it (D buffer 1: rows 32..63); the other rows are the staged block table
+  // and the table, both written before the first MMA; their D lanes are never read.
+  uint8_t qtile[32 * 128];                  // offset 4 KB
   // scaled magnitudes per scale magnitude, 16 interleaved copies (entry e of copy c
   // at 8 (16 e + c) bytes): the 16 threads of an 8-byte wavefront read 16
   // different banks whatever their scales
   uint2 lut[128 * kLutCopies];              // 16 KB
-  int32_t phys[kCtaPages];                  // 4 KB: this CTA's block-table entries (when its range fits)
   uint8_t codes[kStages][kCodeBytes];       // offset 16 KB, 1024-aligned
   uint8_t tile[kBBufs][kTileBytes];         // B operand (SW128), 1024-aligned
   uint8_t scales[kStages][kScaleBytes];
@@ -83,7 +88,8 @@ struct Smem {
   uint32_t taddr;
   uint32_t fma_k[4];                        // 65536, 16: constants the compiler cannot fold
 };
-static_assert(sizeof(uint2) * 128 * kLutCopies >= 96 * 128, "rows 32..127 of the A tile lie in the table");
+static_assert(sizeof(int32_t) * kCtaPages == 32 * 128 && sizeof(uint2) * 128 * kLutCopies >= 96 * 128,
+              "both A tiles lie in the staged block table, the queries and the table");
 static_assert(offsetof(Smem, codes) % 1024 == 0 && offsetof(Smem, tile) % 1024 == 0, "swizzled tiles");
 static_assert(offsetof(Smem, scales) % 16 == 0, "bulk copies need 16-byte alignment");
 
@@ -339,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     PageCursor mm = cursor_at(p0, prefix, B);
     int qtile_req = first_req;
     // K step kk of an operand starts 32 bytes further: +2 in the start-address field
-    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
+    const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(sm.qtile));
+    const uint64_t adesc1 = sdesc_kmajor_sw128(smem_u32(sm.qtile) - 32 * 128);
     const uint32_t tile0 = smem_u32(sm.tile[0]);
     const uint32_t idesc = idesc_e4m3_f32(128, kBlock, false);
     for (int i = 0; i < n; ++i) {
@@ -364,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           tc_fence_after();
           const uint64_t bdesc = sdesc_kmajor_sw128(tile0 + j * kTileBytes);
           const uint32_t d = tbase + k * kDCols;
+          const uint64_t adesc = k == 0 ? adesc0 : adesc1;
 #pragma unroll
           for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ss(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
           mma_commit(smem_u32(&sm.dfull[k]));
@@ -377,9 +385,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     }
     __syncwarp();
-  } else if (warp != 0 && warp != 4) {
+  } else if (warp >= kDqWarp0) {
     // ================= dequant warps: page i -> page tile i % kBBufs, by group i % kDqGroups
-    const int dw = warp == 3 ? 0 : warp - 4, grp = dw >> 2;
+    const int dw = warp - kDqWarp0, grp = dw >> 2;
     const int r = (dw & 3) * 32 + lane;  // token slot within the page = row of the page tile
     const int r7 = r & 7, sw = (r >> 1) & 3;
     const uint32_t row_off = static_cast<uint32_t>(r >> 3) * 1024u + static_cast<uint32_t>(r7) * 128u;
@@ -417,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0) mbar_arrive(smem_u32(&sm.bfull[j]));
     }
   } else {
-    // ================= epilogue warps 0 and 4: pages i = e, e + 2, ... (D buffer e);
-    // lane m = query column rq*4 + g of D
-    const int e = warp >> 2, rq = lane >> 2, g = lane & 3;
+    // ================= epilogue warps 0 and 1: pages i = e, e + 2, ... (D buffer e);
+    // lane m = query column rq*4 + g of D (TMEM lane 32e + m)
+    const int e = warp, rq = lane >> 2, g = lane & 3;
     static_assert(kDBufs == 2, "one D buffer per epilogue warp");
     PageCursor cur = cursor_at(p0 + (e < n ? e : 0), prefix, B);
     for (int i = e; i < n; i += 2) {
@@ -437,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const bool valid = rq < R && !page_bad;
       const int t0 = c * kBlock;
       const int lim = N - R + rq - t0;  // column n of this row is visible iff n <= lim
-      const uint32_t d = tbase + k * kDCols;
+      const uint32_t d = tbase + (static_cast<uint32_t>(32 * e) << 16) + k * kDCols;
       float m = -INFINITY;
 #pragma unroll
       for (int q = 0; q < kBlock / 32; ++q) {
@@ -489,13 +497,24 @@ __global__ void __launch_bounds__(128) topk_kernel(const SelectParams p, int sta
   extern __shared__ float tk_stage[];  // [4][stage_row] block scores (stage_row = 0: read global)
   __shared__ uint64_t scratch[kGroups][64];
   pdl_launch_dependents();
-  pdl_wait_primary();  // the block scores come from the scan kernel
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the request's geometry is an input (not written by the scan): read it before waiting
   const int N = p.context_lens[b];
   const int r0 = p.q_indptr[b], R = p.q_indptr[b + 1] - r0;
+  pdl_wait_primary();  // the block scores come from the scan kernel
+  // stage the 4 whole score rows (16-byte padded) while the geometry loads land
+  if (stage_row > 0) {
+    const int row4 = stage_row / 4;
+    for (int u = threadIdx.x; u < kGroups * row4; u += blockDim.x) {
+      const int g = u / row4, c4 = u - g * row4;
+      reinterpret_cast<float4*>(tk_stage + g * stage_row)[c4] = __ldcg(
+          reinterpret_cast<const float4*>(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride) + c4);
+    }
+  }
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
                   r0 + R <= p.total_rows;
   const int nbb = ok && R > 0 ? (N + kBlock - 1) / kBlock : 0;
+  __syncthreads();
   int32_t* ids = p.block_ids + (static_cast<long long>(b) * kGroups + warp) * kTopK;
   if (nbb == 0) {  // no pages: an empty selection
     if (lane < kTopK) ids[lane] = -1;
@@ -504,18 +523,8 @@ __global__ void __launch_bounds__(128) topk_kernel(const SelectParams p, int sta
         p.block_scores_out[(static_cast<long long>(b) * kGroups + warp) * p.max_pages + c] = -INFINITY;
     return;
   }
-  const bool staged = stage_row >= nbb;
-  if (staged) {
-    const int row4 = (nbb + 3) / 4;  // float4 per group row (block_S rows are 16-byte padded)
-    for (int u = threadIdx.x; u < kGroups * row4; u += blockDim.x) {
-      const int g = u / row4, c4 = u - g * row4;
-      reinterpret_cast<float4*>(tk_stage + g * stage_row)[c4] = __ldcg(
-          reinterpret_cast<const float4*>(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride) + c4);
-    }
-    __syncthreads();
-  }
-  const float* S = staged ? tk_stage + warp * stage_row
-                          : p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
+  const float* S = stage_row > 0 ? tk_stage + warp * stage_row
+                                 : p.block_S + (static_cast<long long>(b) * kGroups + warp) * p.s_stride;
   warp_topk(S, nbb, ids, scratch[warp]);
   if (p.block_scores_out != nullptr) {
     float* o = p.block_scores_out + (static_cast<long long>(b) * kGroups + warp) * p.max_pages;
