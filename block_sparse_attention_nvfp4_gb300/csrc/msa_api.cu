@@ -120,7 +120,6 @@ msa_status check_device(DeviceInfo* d) {
 
 struct Ws {
   uint32_t* flags;
-  uint32_t* req_cnt;
   uint32_t* pair_cnt;
   float* block_S;
   float* part_o;
@@ -133,7 +132,6 @@ msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, const Plan
   if (ws_bytes < L.total) return MSA_ERR_WORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(ws);
   w->flags = reinterpret_cast<uint32_t*>(base + L.flags);
-  w->req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
   w->pair_cnt = reinterpret_cast<uint32_t*>(base + L.pair_cnt);
   w->block_S = reinterpret_cast<float*>(base + L.block_S);
   w->part_o = reinterpret_cast<float*>(base + L.part_o);
@@ -154,7 +152,6 @@ SelectParams select_params(const msa_decode_args* a, const Ws& w, int32_t* ids, 
   p.ki_scale = a->ki_scale;
   p.block_S = w.block_S;
   p.s_stride = score_stride(a->max_pages_per_req);
-  p.req_cnt = w.req_cnt;
   p.flags = w.flags;
   p.block_ids = ids;
   p.block_scores_out = scores_out;
@@ -214,8 +211,6 @@ WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_p
   size_t off = 0;
   L.flags = off;
   off = align_up(off + 16);
-  L.req_cnt = off;
-  off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs));
   L.pair_cnt = off;
   off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs) * kGroups);
   L.block_S = off;

@@ -13,11 +13,11 @@
 // split over the selection). The group's 8R query rows (R speculative rows x 8
 // heads, at most 64) are the rows of a 128-row MMA tile:
 //   * load warp: one lane copies each block's raw NVFP4 K and V (codes and
-//     scales) into a 4-stage shared-memory ring with bulk async copies;
+//     scales) into a 2-stage shared-memory ring with bulk async copies;
 //   * 8 dequant warps, thread = one K row or one V row of the block: dequantise
 //     its 128 elements to E4M3 (byte-permute lookups in a table of scaled
 //     magnitudes) into a 128-byte-swizzled tile (V rows widened to FP16 into two
-//     64-dim tiles); two tile buffers;
+//     64-dim tiles); three tile buffers;
 //   * MMA warp: one lane issues S = Q K^T (FP8; A = query tile, B = K tile, both
 //     shared memory, K-major) into one of two TMEM score buffers, and O += P V
 //     (FP16; A = P from TMEM, B = the V tile read MN-major, so V is used in its
@@ -26,10 +26,12 @@
 //   * 4 softmax warps, two per query row (TMEM lane), each with half of the row's
 //     keys and half of its output dims: read the 64 scores once into registers,
 //     mask, exchange the half maxima through shared memory, online softmax (FP32
-//     running max and sum; exp2 in packed FP16, two keys per instruction, which
-//     is also the FP16 form P takes as the next MMA's A operand in TMEM), and when
-//     the running max grows rescale the row's half of O in TMEM (after the
-//     previous P V has finished). S = Q K^T of block j+1 runs while block j's
+//     running sum; exp2 in packed FP16, two keys per instruction, which is also
+//     the FP16 form P takes as the next MMA's A operand in TMEM). The exponent's
+//     reference point moves only when a block's max exceeds it by more than 2^8
+//     (so P <= 256 stays well inside FP16), and only then is the row's half of O
+//     in TMEM rescaled, after the previous P V has finished; O / l is exact
+//     whatever the reference. S = Q K^T of block j+1 runs while block j's
 //     softmax does.
 // P V runs in FP16: the dequantised V values (E4M3) are exact in FP16, and an
 // E4M3 P (3 mantissa bits) measurably misses 2e-2 relative accuracy on rows whose

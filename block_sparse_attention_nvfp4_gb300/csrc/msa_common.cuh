@@ -102,15 +102,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// Warm L2 with a page that a later TMA copy will read (no shared memory held).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -122,11 +113,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint2 lds_u2(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -156,21 +142,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 16 consecutive 32-bit TMEM columns of this thread's lane <- v[0..15]
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-// v[0..31] <- 32 consecutive 32-bit TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -259,16 +230,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// ---------------------------------------------------------------- warp MMA (legacy path)
-// D(16x8, f32) += A(16x32, e4m3) * B(32x8, e4m3)
-__device__ __forceinline__ void mma_m16n8k32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                             uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // ---------------------------------------------------------------- NVFP4 -> E4M3
 // [vLLM-zh, Blackwell kernels] the cache is NVFP4 while queries are FP8, so the
 // kernels turn NVFP4 into FP8 before an FP8 MMA. The FP8 value of an element is
@@ -277,12 +238,6 @@ __device__ __forceinline__ void mma_m16n8k32(float (&d)[4], uint32_t a0, uint32_
 // via table lookup]: 256 scales x 8 magnitudes, pre-rounded to FP8). Here each
 // CTA builds it in shared memory with the hardware conversions and byte-permute
 // instructions do four lookups at a time.
-//
-// Entry for scale s (16 bytes): x,y = magnitude bytes |E4M3(m_c * s)| for
-// c = 0..7; z,w = the same bytes in reverse order (index 7-c).
-struct LutEntry {
-  uint32_t p0, p1, n0, n1;
-};
 
 __device__ __forceinline__ uint32_t cvt_e2m1x2_scaled(uint32_t byte_pair, uint32_t scale_h2) {
   uint32_t h;
@@ -304,18 +259,6 @@ __device__ __forceinline__ uint2 lut_magnitudes(uint32_t s) {
   const uint32_t sc = e4m3_to_h2_bcast(s & 0x7Fu);
   return make_uint2(cvt_e2m1x2_scaled(0x10, sc) | (cvt_e2m1x2_scaled(0x32, sc) << 16),
                     cvt_e2m1x2_scaled(0x54, sc) | (cvt_e2m1x2_scaled(0x76, sc) << 16));
-}
-// One entry per thread of the block; 256 entries.
-__device__ __forceinline__ void build_lut(LutEntry* lut) {
-  for (int s = threadIdx.x; s < 256; s += blockDim.x) {
-    const uint2 m = lut_magnitudes(static_cast<uint32_t>(s));
-    LutEntry e;
-    e.p0 = m.x;
-    e.p1 = m.y;
-    e.n0 = __byte_perm(m.y, 0, 0x0123);
-    e.n1 = __byte_perm(m.x, 0, 0x0123);
-    lut[s] = e;
-  }
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -339,23 +282,6 @@ __device__ __forceinline__ void dq8_signed(uint32_t w, uint32_t L0, uint32_t L1,
   r1 = m1 ^ (s1 & 0x80808080u);
 }
 
-// Split form for the index scan: positive-part bytes p (magnitude where the
-// element is positive, 0 where negative) and negative-part bytes n (magnitude
-// where negative, 0 where positive), so k = p - n elementwise. The byte permute
-// in its default mode turns a selector nibble with bit 3 set into the sign
-// replicate of the chosen byte, which is 0 for these (non-negative) table bytes:
-// the raw code nibble picks the magnitude of positive elements and zeroes
-// negative ones; the complemented nibble (sign flipped, index 7-c into the
-// reversed table) does the opposite. The MMA then subtracts the n part by
-// negating its B operand.
-__device__ __forceinline__ void dq8_split(uint32_t w, const LutEntry& L, uint32_t& p0, uint32_t& p1, uint32_t& n0,
-                                          uint32_t& n1) {
-  const uint32_t wh = w >> 16;
-  p0 = prmt(L.p0, L.p1, w);
-  p1 = prmt(L.p0, L.p1, wh);
-  n0 = prmt(L.n0, L.n1, ~w);
-  n1 = prmt(L.n0, L.n1, ~wh);
-}
 
 // ---------------------------------------------------------------- top-k
 // [vLLM-zh §How; MSA-fig §1 TopK] One warp selects the blocks of one group:
@@ -386,10 +312,6 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
   const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), m);
   const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), m);
   return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-// Value of candidate slot c (c < nc) as a key; 0 (below every real key) past the end.
-__device__ __forceinline__ uint64_t cand_key(const float* S, int c, int nc) {
-  return c < nc ? topk_key(S[c], c) : 0ull;
 }
 
 // Warp-wide descending bitonic sort of one u64 per lane.

@@ -18,7 +18,6 @@ struct SelectParams {
   const uint8_t* ki_scale;
   float* block_S;           // workspace [B][4][s_stride] block scores
   int s_stride;             // max_pages rounded up to a multiple of 4 (16-byte rows)
-  uint32_t* req_cnt;        // workspace [B] (unused by the kernels; kept in the layout)
   uint32_t* flags;          // workspace error flags
   int32_t* block_ids;       // [B][4][16]
   float* block_scores_out;  // optional [B][4][max_pages]
@@ -65,7 +64,7 @@ struct AttnParams {
 
 // Workspace layout, offsets in bytes (each 256-aligned).
 struct WsLayout {
-  size_t flags, req_cnt, pair_cnt, block_S, part_o, part_lse2, total;
+  size_t flags, pair_cnt, block_S, part_o, part_lse2, total;
 };
 
 struct Plan {

@@ -1,14 +1,14 @@
-// msa_select_blocks_noalloc: the fused block selection (index scan, block max
-// pool, top-k) for callers that cannot allocate device memory.
+// msa_select_blocks_noalloc: the block selection (index scan with block max
+// pool, then top-k) for callers that cannot allocate device memory.
 //
 // Who needs this: some hosts give a library only the tensors it works on and
 // keep the device allocator to themselves (plugin and custom-operator
 // interfaces of inference servers, sandboxed extensions), and some decode loops
 // must not call cudaMalloc at all, because it can synchronise the device and
 // stall every other stream. Such callers cannot provide the workspace that
-// msa_select_blocks takes. This entry point runs the same kernel with its
-// scratch (device error flags, per-request arrival counters, block scores) in
-// a fixed buffer compiled into the library instead.
+// msa_select_blocks takes. This entry point runs the same kernels with their
+// scratch (device error flags, block scores) in a fixed buffer compiled into
+// the library instead.
 //
 // The buffer is kScratchBytes (8 MiB) of device memory that every GPU which
 // loads libmsa holds until the process exits. All calls share it, so calls that
@@ -53,8 +53,6 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
 }  // namespace
 }  // namespace msa
 
@@ -79,9 +77,8 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
       (reinterpret_cast<uintptr_t>(args->ki_scale) & 15u))
     return MSA_ERR_INVALID_ARG;
 
-  // scratch layout: error flags | arrival counters [B] | block scores [B][4][max_pages rounded up to 4]
-  const size_t off_cnt = 256;
-  const size_t off_S = align256(off_cnt + sizeof(uint32_t) * static_cast<size_t>(args->num_reqs));
+  // scratch layout: error flags (256 B) | block scores [B][4][max_pages rounded up to 4]
+  const size_t off_S = 256;
   const size_t need =
       off_S + sizeof(float) * static_cast<size_t>(args->num_reqs) * kGroups * score_stride(args->max_pages_per_req);
   if (need > kScratchBytes) return MSA_ERR_WORKSPACE;  // the batch needs more than the fixed buffer holds
@@ -99,7 +96,7 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* s = static_cast<uint8_t*>(base);
-  // flags and counters must start at zero; the block maxima are written before they are read
+  // the flags must start at zero; the block maxima are written before they are read
   if (cudaMemsetAsync(s, 0, off_S, st) != cudaSuccess) return MSA_ERR_CUDA;
 
   CUtensorMap map;
@@ -133,7 +130,6 @@ extern "C" msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int
   p.q_idx = args->q_idx;
   p.ki_scale = args->ki_scale;
   p.flags = reinterpret_cast<uint32_t*>(s);
-  p.req_cnt = reinterpret_cast<uint32_t*>(s + off_cnt);
   p.block_S = reinterpret_cast<float*>(s + off_S);
   p.s_stride = score_stride(args->max_pages_per_req);
   p.block_ids = block_ids;

@@ -25,17 +25,20 @@
 //     read back) and P the dequantised page (N = 128 tokens, K = 128), FP32
 //     accumulation in tensor memory (products of two E4M3 values are exact; only
 //     the FP32 sums round); the warp rewrites Q when the request changes;
-//   * 2 epilogue warps taking alternate pages (TMEM lanes 0..31 = the 32 query
-//     columns rq*4+g): read the page's 32 x 128 scores, mask, take each row's
-//     maximum over the tokens and the group's maximum over its rows with
-//     shuffles, and write the block score.
+//   * 2 epilogue warps taking alternate pages (D buffer e, TMEM lanes
+//     32e..32e+31 = the 32 query columns rq*4+g): read the page's 32 x 128
+//     scores, mask, take each row's maximum over the tokens and the group's
+//     maximum over its rows with shuffles, and write the block score.
 // Laying the scores out with the query columns on TMEM lanes puts a whole page's
 // max pool in one warp (no cross-warp combine); measured on GB300, the pool was
 // the costliest step when the 128 tokens were spread over four warps' lanes.
 // The dequant warps never wait for an MMA result, only for a free page tile, so
-// the MMA round trip hides behind the next pages' dequantisation. The CTA that
-// completes a request's block scores (an arrival counter, no waiting) runs the
-// top-k for that request: one warp per group.
+// the MMA round trip hides behind the next pages' dequantisation.
+//
+// The top-k runs in a second kernel (one CTA per request, one warp per group),
+// launched with programmatic dependent launch so its CTAs are resident and have
+// read the request geometry when the scan's last pages finish; it waits on the
+// scan's completion (griddepcontrol.wait), not on any flag another CTA writes.
 #include <climits>
 #include <cstddef>
 
@@ -574,36 +577,30 @@ __global__ void __launch_bounds__(128) maxpool_topk_kernel(const MaxpoolParams p
   }
 }
 
-// Exposes the two dequantisers for checking.
+// Exposes the kernels' dequantisers for checking: path 0 = dq8_signed, the
+// attention kernel's form (its K operand, and V before the exact E4M3 -> FP16
+// widening); path 1 = dq8_signed_fma, the index scan's form.
 __global__ void dequant_rows_kernel(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out,
                                     int path) {
-  __shared__ LutEntry lut[256];
-  build_lut(lut);
+  __shared__ uint2 lut[128];
+  __shared__ uint32_t fma_k[2];
+  for (int s = threadIdx.x; s < 128; s += blockDim.x) lut[s] = lut_magnitudes(static_cast<uint32_t>(s));
+  if (threadIdx.x == 0) {
+    fma_k[0] = 65536u;
+    fma_k[1] = 16u;
+  }
   __syncthreads();
+  const uint32_t k16 = fma_k[0], k4 = fma_k[1];
   const long long nwords = nrows * 16;
   for (long long u = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; u < nwords;
        u += static_cast<long long>(gridDim.x) * blockDim.x) {
     const long long row = u >> 4;
     const int wi = static_cast<int>(u & 15);
     const uint32_t w = *reinterpret_cast<const uint32_t*>(codes + row * 64 + wi * 4);
-    const LutEntry L = lut[scales[row * 8 + wi / 2]];
+    const uint2 L = lut[scales[row * 8 + wi / 2] & 0x7Fu];
     uint32_t r0, r1;
-    if (path == 0) {
-      dq8_signed(w, L.p0, L.p1, r0, r1);
-    } else {
-      uint32_t p0, p1, n0, n1;
-      dq8_split(w, L, p0, p1, n0, n1);
-      // recombine: positive part where non-zero, else the negative part with its sign bit
-      r0 = 0;
-      r1 = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t a0 = (p0 >> (8 * k)) & 0xFFu, b0 = (n0 >> (8 * k)) & 0xFFu;
-        const uint32_t a1 = (p1 >> (8 * k)) & 0xFFu, b1 = (n1 >> (8 * k)) & 0xFFu;
-        r0 |= (a0 != 0 ? a0 : (b0 != 0 ? (b0 | 0x80u) : 0u)) << (8 * k);
-        r1 |= (a1 != 0 ? a1 : (b1 != 0 ? (b1 | 0x80u) : 0u)) << (8 * k);
-      }
-    }
+    if (path == 0) dq8_signed(w, L.x, L.y, r0, r1);
+    else dq8_signed_fma(w, L.x, L.y, k16, k4, r0, r1);
     *reinterpret_cast<uint32_t*>(out + row * 128 + wi * 8) = r0;
     *reinterpret_cast<uint32_t*>(out + row * 128 + wi * 8 + 4) = r1;
   }

@@ -145,9 +145,11 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
                                   int32_t* block_ids, float* block_scores,
                                   void* ws, size_t ws_bytes, void* stream);
 
-/* Steps 1+2+3 fused: one streaming pass over the index-key cache with the block
- * max pool and the top-k in its epilogue; per-token scores never reach memory.
- * Outputs as msa_block_maxpool_topk. This is the first kernel of msa_decode. */
+/* Steps 1+2+3: one streaming pass over the index-key cache with the block max
+ * pool in its epilogue (per-token scores never reach memory; block maxima go to
+ * the workspace), then a top-k kernel chained to it by programmatic dependent
+ * launch. Outputs as msa_block_maxpool_topk. These are the first two kernels of
+ * msa_decode. */
 msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
                              void* ws, size_t ws_bytes, void* stream);
 
@@ -162,32 +164,32 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* bl
  * pages have no counterpart to this entry point; it exists for hosts that hand a
  * library only the tensors it works on and keep the allocator to themselves
  * (plugin / custom-operator interfaces), and for decode loops that must not call
- * cudaMalloc because it can synchronise the device. It runs the same kernel as
- * msa_select_blocks with the same outputs, but its scratch (error flags, arrival
- * counters, block scores: 256 + 4*B rounded up to 256, plus 16*B*P4 bytes where P4 is
- * max_pages_per_req rounded up to a multiple of 4) lives in a fixed 8 MiB device
- * buffer inside the library, which every
- * GPU that loads libmsa holds until the process exits. Batches needing more return
+ * cudaMalloc because it can synchronise the device. It runs the same kernels as
+ * msa_select_blocks with the same outputs, but its scratch (error flags and block
+ * scores: 256 + 16*B*P4 bytes, where P4 is max_pages_per_req rounded up to a
+ * multiple of 4) lives in a fixed 8 MiB device buffer inside the library, which
+ * every GPU that loads libmsa holds until the process exits. Batches needing more return
  * MSA_ERR_WORKSPACE before any launch. It allocates nothing: the first call on each
  * device looks the buffer's address up once (make that first call before any
- * stream capture), and every call clears the flags and counters with an async
- * memset on `stream`. All calls share the one buffer, so calls that overlap on the
+ * stream capture), and every call clears the flags with an async memset on
+ * `stream`. All calls share the one buffer, so calls that overlap on the
  * GPU (other streams, other host threads) race and must be serialised by the
  * caller. Device error flags are cleared per call and not reported. */
 msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
                                      void* stream);
 
-/* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, the
- * second launch chained to the first with programmatic dependent launch. */
+/* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, three
+ * kernels on `stream`, each chained to the one before it with programmatic
+ * dependent launch. */
 msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse,
                       void* ws, size_t ws_bytes, void* stream);
 
 /* The dequantisers the kernels use, exposed for checking: rows of 128 NVFP4
  * elements (codes [n][64], scales [n][8]) -> E4M3 bytes out_e4m3 [n][128], element
- * j of row i at out_e4m3[i*128 + j]. path 0 = the signed form the attention
- * kernel feeds its MMA; path 1 = the index scan's form, which splits each row
- * into positive and negative magnitude parts (recombined here into one signed
- * byte; a zero may come back as either sign).
+ * j of row i at out_e4m3[i*128 + j]. path 0 = the form of the attention
+ * kernel (its K operand, and V before an exact E4M3 -> FP16 widening); path 1 =
+ * the index scan's form (the same table, shifts done as multiplies). The scale
+ * byte's sign bit is ignored.
  * [vLLM-zh, Blackwell kernels: NVFP4 turned into FP8 before the FP8 MMA] */
 msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t nrows,
                             uint8_t* out_e4m3, int32_t path, void* stream);
