@@ -49,50 +49,66 @@ namespace msa {
 
 namespace {
 
-// Warp roles. Warp w runs on SM sub-partition w % 4 and reads TMEM lanes
-// 32 (w % 4) .. + 31. D buffer e holds the 32 query columns in lanes 32e .. 32e + 31
-// (its A tile starts 32 rows earlier for e = 1), so epilogue warps 0 and 1 read
-// buffers 0 and 1 (pages i with i % 2 = e), and every sub-partition runs one warp of
-// each dequant group plus one of: epilogue, epilogue, load, MMA (measured on GB300:
-// with 3 of the 8 dequant warps on one sub-partition, those lagged the group).
-constexpr int kLoadWarp = 2;   // TMA producer
-constexpr int kIssueWarp = 3;  // MMA issue, query tile, TMEM allocation
-constexpr int kDqWarp0 = 4;    // dequant warps 4..11: group (w - 4) / 4, one warp per sub-partition
-constexpr int kDqGroups = 2;   // page i is dequantised by group i % kDqGroups
+// Warp roles. Warp w runs on SM sub-partition w % 4 and may read TMEM lanes
+// 32 (w % 4) .. + 31. The scores of a page come from the weight-stationary MMA with
+// M = 32 (the query columns), whose D puts rows 0..31 in every lane quadrant and the
+// page's tokens 32q .. 32q + 31 in quadrant q (32 TMEM columns per page). Four pool
+// warps, one per quadrant, reduce a page with the TMEM load's max reduction; each
+// dequant group has one warp per sub-partition, so the ALU-heavy work is spread
+// evenly. One thread issues an MMA only every ~45-64 cycles (measured on GB300), so
+// two MMA warps take alternate pages, each with its own copy of the query tile, and
+// so do two load warps. One CTA per SM: the register file holds 24 warps at up to 85
+// registers.
+constexpr int kLoadWarp = 0;   // TMA producer (even pages)
+constexpr int kIssueWarp = 1;  // MMA issue (even pages), query tile 0, TMEM allocation
+constexpr int kPoolWarp0 = 2;  // pool warps 2..9: set (w - 2) / 4 takes pages of its parity
+constexpr int kPoolSets = 2;
+constexpr int kDqWarp0 = kPoolWarp0 + 4 * kPoolSets;  // dequant warps 10..25: group (w - 10) / 4
+constexpr int kDqGroups = 4;   // page i is dequantised by group i % kDqGroups
 constexpr int kDqWarps = 4 * kDqGroups;
-constexpr int kThreads = (kDqWarp0 + kDqWarps) * 32;
-constexpr int kCtasPerSm = 2;
-constexpr int kStages = 4, kBBufs = 3, kDBufs = 2;
+constexpr int kIssueWarp2 = kDqWarp0 + kDqWarps;  // MMA issue (odd pages), query tile 1
+constexpr int kIssuers = 2;
+constexpr int kLoadWarp2 = kIssueWarp2 + 1;       // TMA producer (odd pages)
+constexpr int kLoaders = 2;
+constexpr int kThreads = (kLoadWarp2 + 1) * 32;
+constexpr int kPoolBatch = 4;  // a pool set's own pages per cross-quadrant combine
+constexpr int kCtasPerSm = 1;
+constexpr int kStages = 8, kBBufs = 4, kDBufs = 16;
+// Every ring slot must have one in-order producer and one in-order consumer, or a
+// parity wait could pass on a phase two uses old: a stage is filled by one load warp
+// and read by one dequant group, a page tile written by one group and read by one MMA
+// warp, a D buffer written by one MMA warp (and read in order by all pool warps).
+static_assert(kStages % kLoaders == 0 && kStages % kDqGroups == 0, "stage ring");
+static_assert(kBBufs % kIssuers == 0 && kBBufs % kDqGroups == 0, "page-tile ring");
+static_assert(kDBufs % kIssuers == 0 && kDBufs % kPoolSets == 0, "D-buffer ring");
 constexpr uint32_t kCodeBytes = kBlock * 64;    // one page of index-key codes
 constexpr uint32_t kScaleBytes = kBlock * 8;    // its scales
 constexpr uint32_t kTileBytes = kBlock * kDim;  // one dequantised page (E4M3)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kDCols = kBlock;             // D buffer: 128 FP32 columns (tokens)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCols = 32;                 // D buffer: 32 FP32 columns x 4 lane quadrants
 constexpr int kCtaPages = 1024;                 // block-table entries staged per CTA
 constexpr int kLutCopies = 16;                  // one per thread of a 16-thread (8-byte) wavefront
 static_assert(kDBufs * kDCols <= kTmemCols, "TMEM buffers exceed the allocation");
+static_assert(kDqWarp0 % 4 == 2 && kPoolWarp0 % 4 == 2, "each group of four warps covers the four lane quadrants");
 
 struct Smem {
   int32_t phys[kCtaPages];                  // offset 0, 4 KB: this CTA's block-table entries (when they fit)
-  // A operand: the request's index queries, 32 rows of 128 bytes. The MMA reads a
-  // 128-row tile starting at qtile (D buffer 0: queries in rows 0..31) or 32 rows
-  // before it (D buffer 1: rows 32..63); the other rows are the staged block table
-  // and the table, both written before the first MMA; their D lanes are never read.
-  uint8_t qtile[32 * 128];                  // offset 4 KB
+  uint8_t qtile[kIssuers][32 * 128];        // offset 4 KB: A operands, one per MMA warp: index queries (SW128)
   // scaled magnitudes per scale magnitude, 16 interleaved copies (entry e of copy c
   // at 8 (16 e + c) bytes): the 16 threads of an 8-byte wavefront read 16
   // different banks whatever their scales
   uint2 lut[128 * kLutCopies];              // 16 KB
-  uint8_t codes[kStages][kCodeBytes];       // offset 16 KB, 1024-aligned
+  uint8_t codes[kStages][kCodeBytes];       // offset 24 KB, 1024-aligned
   uint8_t tile[kBBufs][kTileBytes];         // B operand (SW128), 1024-aligned
   uint8_t scales[kStages][kScaleBytes];
+  float part[kDBufs][4][kGroups];           // per D buffer: the pool warps' quadrant maxima per index group
+  int2 page_bc[kDBufs];                     // per D buffer: (request, block) of its page
   uint64_t full[kStages], empty[kStages];
   uint64_t bfull[kBBufs], bfree[kBBufs], dfull[kDBufs], dempty[kDBufs];
   uint32_t taddr;
   uint32_t fma_k[4];                        // 65536, 16: constants the compiler cannot fold
 };
-static_assert(sizeof(int32_t) * kCtaPages == 32 * 128 && sizeof(uint2) * 128 * kLutCopies >= 96 * 128,
-              "both A tiles lie in the staged block table, the queries and the table");
+static_assert(offsetof(Smem, qtile) % 1024 == 0, "swizzled A tile");
 static_assert(offsetof(Smem, codes) % 1024 == 0 && offsetof(Smem, tile) % 1024 == 0, "swizzled tiles");
 static_assert(offsetof(Smem, scales) % 16 == 0, "bulk copies need 16-byte alignment");
 
@@ -101,9 +117,11 @@ struct PageCursor {
   int c;       // logical block within the request
 };
 
-__device__ __forceinline__ void cursor_advance(PageCursor& pc, const int* nb) {
+// prefix[b] = the first page of request b in the concatenation of all requests'
+// pages; prefix[B + 1] is a sentinel far beyond prefix[B] that stops the walk.
+__device__ __forceinline__ void cursor_advance(PageCursor& pc, const long long* prefix) {
   ++pc.c;
-  while (pc.c >= nb[pc.b]) {
+  while (pc.c >= prefix[pc.b + 1] - prefix[pc.b]) {
     pc.c = 0;
     ++pc.b;
   }
@@ -131,19 +149,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float m;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
   return m;
-}
-
-// Maximum of 32 scores (one tcgen05 load): 4 independent chains.
-__device__ __forceinline__ float max32(const uint32_t (&v)[32]) {
-  float acc[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    float a = fmax3(__uint_as_float(v[u]), __uint_as_float(v[4 + u]), __uint_as_float(v[8 + u]));
-    a = fmax3(a, __uint_as_float(v[12 + u]), __uint_as_float(v[16 + u]));
-    a = fmax3(a, __uint_as_float(v[20 + u]), __uint_as_float(v[24 + u]));
-    acc[u] = fmaxf(a, __uint_as_float(v[28 + u]));
-  }
-  return fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
 }
 
 // Maximum over the visible columns n <= lim of 32 scores starting at column n0.
@@ -213,11 +218,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem_al = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // TMA/UMMA tiles need 1 KB
   Smem& sm = *reinterpret_cast<Smem*>(smem_al);
-  long long* prefix = reinterpret_cast<long long*>(smem_al + sizeof(Smem));  // [B+1]
-  int* nb = reinterpret_cast<int*>(prefix + (p.num_reqs + 1));              // [B+1] (sentinel)
-  int* rows_s = nb + (p.num_reqs + 1);                                     // [B]
-  int* row0_s = rows_s + p.num_reqs;                                        // [B]
-  int* ctx_s = row0_s + p.num_reqs;                                         // [B]
+  // page prefix over requests [B + 2]: counts first, then scanned in place. Only
+  // requests that passed the checks below own pages, so the geometry of a page's
+  // request is read from the (validated) inputs where it is needed.
+  long long* prefix = reinterpret_cast<long long*>(smem_al + sizeof(Smem));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.num_reqs;
@@ -237,18 +241,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       pages = 0;
     }
     if (R == 0) pages = 0;
-    nb[b] = pages;
-    rows_s[b] = ok ? R : 0;
-    row0_s[b] = ok ? r0 : 0;
-    ctx_s[b] = ok ? N : 0;
+    prefix[b] = pages;
   }
-  if (tid == 0) nb[B] = 1 << 30;  // sentinel stops cursor walks
   __syncthreads();
   if (warp == 0) {  // exclusive prefix over requests: each lane scans a contiguous chunk
     const int per = (B + 31) / 32;
     const int b0 = min(lane * per, B), b1 = min(b0 + per, B);
     long long part = 0;
-    for (int b = b0; b < b1; ++b) part += nb[b];
+    for (int b = b0; b < b1; ++b) part += prefix[b];
     long long incl = part;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -257,10 +257,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     long long acc = incl - part;
     for (int b = b0; b < b1; ++b) {
+      const long long cnt = prefix[b];
       prefix[b] = acc;
-      acc += nb[b];
+      acc += cnt;
     }
-    if (lane == 31) prefix[B] = incl;
+    if (lane == 31) {
+      prefix[B] = incl;
+      prefix[B + 1] = incl + (1LL << 40);  // sentinel
+    }
   }
   __syncthreads();
   const long long total = prefix[B];
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     for (int k = 0; k < kDBufs; ++k) {
       mbar_init(smem_u32(&sm.dfull[k]), 1);
-      mbar_init(smem_u32(&sm.dempty[k]), 1);
+      mbar_init(smem_u32(&sm.dempty[k]), 4);  // the 4 warps (lane quadrants) of the pooling group
     }
     mbar_fence_init();
   }
@@ -299,7 +303,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   // the first request's index queries
   const int first_req = cursor_at(p0, prefix, B).b;
-  write_qtile(sm.qtile, p.q_idx, row0_s[first_req], rows_s[first_req], tid, kThreads);
+  for (int m = 0; m < kIssuers; ++m)
+    write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[first_req], p.q_indptr[first_req + 1] - p.q_indptr[first_req], tid,
+                kThreads);
   fence_proxy_async_smem();
   if (warp == kIssueWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
@@ -308,12 +314,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   const uint32_t tbase = sm.taddr;
   bool alive = true;
 
-  if (warp == kLoadWarp) {
-    // ================= load warp: TMA producer (one lane)
+  if (warp == kLoadWarp || warp == kLoadWarp2) {
+    // ================= load warps: TMA producers (one lane each), warp L takes pages L, L + 2, ...
+    const int L = warp == kLoadWarp ? 0 : 1;
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&ki_map)) : "memory");
-      PageCursor ld = cursor_at(p0, prefix, B);
-      for (int i = 0; i < n; ++i) {
+      PageCursor ld = cursor_at(p0 + (L < n ? L : 0), prefix, B);
+      for (int i = L; i < n; i += kLoaders) {
         const int s = i % kStages;
 
         if (i >= kStages) {  // the dequant group has released this stage's previous page
@@ -332,37 +339,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           bulk_load(smem_u32(sm.scales[s]), p.ki_scale + static_cast<long long>(phys) * kScaleBytes, kScaleBytes,
                     bar);
         }
-        cursor_advance(ld, nb);
+        cursor_advance(ld, prefix);
+        cursor_advance(ld, prefix);
       }
       if (!alive) {
         // drain: copies already issued complete on their own barriers
-        for (int i = 0; i < n; ++i) {
+        for (int i = L; i < n; i += kLoaders) {
           const int s = i % kStages;
           if (!mbar_wait(smem_u32(&sm.full[s]), (i / kStages) & 1, p.flags)) break;
         }
       }
     }
     __syncwarp();
-  } else if (warp == kIssueWarp) {
-    // ================= MMA warp: MMA issue (lane 0), query tile (all lanes)
-    PageCursor mm = cursor_at(p0, prefix, B);
+  } else if (warp == kIssueWarp || warp == kIssueWarp2) {
+    // ================= MMA warps: warp m issues pages m, m + 2, ... (lane 0) and keeps
+    // its own query tile (all lanes)
+    const int m = warp == kIssueWarp ? 0 : 1;
+    PageCursor mm = cursor_at(p0 + (m < n ? m : 0), prefix, B);
+    int nbc = static_cast<int>(prefix[mm.b + 1] - prefix[mm.b]);  // pages of the cursor's request
     int qtile_req = first_req;
     // K step kk of an operand starts 32 bytes further: +2 in the start-address field
-    const uint64_t adesc0 = sdesc_kmajor_sw128(smem_u32(sm.qtile));
-    const uint64_t adesc1 = sdesc_kmajor_sw128(smem_u32(sm.qtile) - 32 * 128);
+    const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sm.qtile[m]));
     const uint32_t tile0 = smem_u32(sm.tile[0]);
-    const uint32_t idesc = idesc_e4m3_f32(128, kBlock, false);
-    for (int i = 0; i < n; ++i) {
+    const uint32_t idesc = idesc_e4m3_f32(32, kBlock, false);
+    for (int i = m; i < n; i += kIssuers) {
       const int j = i % kBBufs, k = i % kDBufs;
       if (mm.b != qtile_req) {
-        // new request: once every earlier MMA has finished reading the tile, rewrite it
-        if (i >= 1) alive = wait_bar(smem_u32(&sm.dfull[(i - 1) % kDBufs]), ((i - 1) / kDBufs) & 1, p.flags);
+        // new request: once this warp's earlier MMAs have finished reading its tile, rewrite it
+        const int ip = i - kIssuers;
+        if (ip >= 0) alive = wait_bar(smem_u32(&sm.dfull[ip % kDBufs]), (ip / kDBufs) & 1, p.flags);
         if (!__all_sync(0xFFFFFFFFu, alive)) {
           alive = false;
           break;
         }
         tc_fence_after();
-        write_qtile(sm.qtile, p.q_idx, row0_s[mm.b], rows_s[mm.b], lane, 32);
+        write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[mm.b], p.q_indptr[mm.b + 1] - p.q_indptr[mm.b], lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         qtile_req = mm.b;
@@ -374,21 +385,115 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           tc_fence_after();
           const uint64_t bdesc = sdesc_kmajor_sw128(tile0 + j * kTileBytes);
           const uint32_t d = tbase + k * kDCols;
-          const uint64_t adesc = k == 0 ? adesc0 : adesc1;
 #pragma unroll
-          for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ss(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
+          for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ws(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
           mma_commit(smem_u32(&sm.dfull[k]));
           mma_commit(smem_u32(&sm.bfree[j]));
         }
       }
-      cursor_advance(mm, nb);
-      if (!__all_sync(0xFFFFFFFFu, alive)) {
-        alive = false;
-        break;
+      for (int u = 0; u < kIssuers; ++u) {
+        if (++mm.c >= nbc) {  // the next request with pages (the sentinel ends the walk)
+          mm.c = 0;
+          do ++mm.b;
+          while (prefix[mm.b + 1] == prefix[mm.b]);
+          nbc = static_cast<int>(prefix[mm.b + 1] - prefix[mm.b]);
+        }
       }
+      alive = __shfl_sync(0xFFFFFFFFu, alive ? 1 : 0, 0) != 0;  // lane 0 waited and issued
+      if (!alive) break;
     }
     __syncwarp();
-  } else if (warp >= kDqWarp0) {
+  } else if (warp < kDqWarp0) {
+    // ================= pool warps: set P takes pages i = P, P + kPoolSets, ... from D
+    // buffer k = i % kDBufs. The warp's lane quadrant q = warp % 4 holds the page's tokens
+    // 32q .. 32q + 31 (lane m = query column rq * 4 + g). Each warp leaves its quadrant's
+    // group maxima in slot k; every kPoolBatch of its pages the set's four warps meet at
+    // the set's named barrier and its quadrant-0 warp combines the batch (lane = page *
+    // 4 + group). A slot is rewritten only after the set's next barrier. All four run the
+    // same number of steps and barriers, timeouts included, so the barrier always completes.
+    static_assert(kPoolBatch * kGroups <= 32 && kDBufs >= 2 * kPoolBatch * kPoolSets, "pool slot reuse");
+    const int set = (warp - kPoolWarp0) >> 2, quad = warp & 3, rq = lane >> 2, g = lane & 3;
+    const uint32_t d_lane = tbase + (static_cast<uint32_t>(32 * quad) << 16);
+    PageCursor pc = cursor_at(p0 + (set < n ? set : 0), prefix, B);
+    int nbc = static_cast<int>(prefix[pc.b + 1] - prefix[pc.b]);  // pages of the cursor's request
+    // the page's request geometry, reloaded only when the request changes
+    int cur_b = -1, N = 0, row0 = 0, R = 0;
+    int it = 0;
+    for (int ip = set; ip < n; ip += kPoolSets, ++it) {
+      const int k = ip % kDBufs;
+      if (pc.b != cur_b) {
+        cur_b = pc.b;
+        N = p.context_lens[cur_b];
+        row0 = p.q_indptr[cur_b];
+        R = p.q_indptr[cur_b + 1] - row0;
+      }
+      if (alive) alive = wait_bar(smem_u32(&sm.dfull[k]), (ip / kDBufs) & 1, p.flags);
+      alive = __all_sync(0xFFFFFFFFu, alive) != 0;
+      tc_fence_after();
+      const int b = pc.b, c = pc.c;
+      const int t0 = c * kBlock + 32 * quad;  // this quadrant's first token
+      const int lim = N - R + rq - t0;        // column u is visible to this row iff u <= lim
+      const uint32_t d = d_lane + static_cast<uint32_t>(k) * kDCols;
+      float m = -INFINITY;
+      if (alive) {
+        if (MODE == 0 && N - R - t0 >= 31) {
+          // every row sees the quadrant's 32 tokens (a warp-uniform test): the load's own
+          // max reduction gives each row's maximum
+          const float mq = tmem_ld32_max(d);
+          tc_wait_ld();
+          if (rq < R) m = mq;
+        } else {
+          uint32_t v[32];
+          tmem_ld32(d, v);
+          tc_wait_ld();
+          if (MODE == 0) {
+            if (rq < R) m = max32_masked(v, 0, lim);
+          } else if (rq < R) {
+            const int phys = staged ? sm.phys[ip] : p.block_table[static_cast<long long>(b) * p.max_pages + c];
+            const bool page_bad = phys < 0 || phys >= p.num_pages;
+            float* out = p.token_scores + (static_cast<long long>(row0 + rq) * kGroups + g) * p.score_stride + t0;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+              if (t0 + u < N) out[u] = !page_bad && u <= lim ? __uint_as_float(v[u]) : -INFINITY;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
+      if (MODE == 0) {
+        // the group's maximum over its rows: lanes with equal lane % 4
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        if (lane < kGroups) sm.part[k][quad][lane] = m;
+        if (quad == 0 && lane == 0) sm.page_bc[k] = make_int2(b, c);
+        if ((it + 1) % kPoolBatch == 0 || ip + kPoolSets >= n) {
+          named_bar_sync(1 + set, 128);
+          const int pg = ip - kPoolSets * (it % kPoolBatch) + kPoolSets * (lane >> 2);
+          if (quad == 0 && lane < kPoolBatch * kGroups && pg <= ip) {
+            const int kk = pg % kDBufs;
+            const int2 bc = sm.page_bc[kk];
+            // a page whose table entry is out of range scores -inf (its codes were never loaded)
+            const int phys = staged ? sm.phys[pg] : p.block_table[static_cast<long long>(bc.x) * p.max_pages + bc.y];
+            const float mm = phys < 0 || phys >= p.num_pages
+                                 ? -INFINITY
+                                 : fmaxf(fmax3(sm.part[kk][0][g], sm.part[kk][1][g], sm.part[kk][2][g]),
+                                         sm.part[kk][3][g]);
+            p.block_S[(static_cast<long long>(bc.x) * kGroups + g) * p.s_stride + bc.y] = alive ? mm : -INFINITY;
+          }
+        }
+      }
+      for (int u = 0; u < kPoolSets; ++u) {
+        if (++pc.c >= nbc) {  // the next request with pages (the sentinel ends the walk)
+          pc.c = 0;
+          do ++pc.b;
+          while (prefix[pc.b + 1] == prefix[pc.b]);
+          nbc = static_cast<int>(prefix[pc.b + 1] - prefix[pc.b]);
+        }
+      }
+    }
+  } else {
     // ================= dequant warps: page i -> page tile i % kBBufs, by group i % kDqGroups
     const int dw = warp - kDqWarp0, grp = dw >> 2;
     const int r = (dw & 3) * 32 + lane;  // token slot within the page = row of the page tile
@@ -405,12 +510,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // this thread's row: 64 code bytes (swizzled 16-byte chunks) + 8 scale bytes
       const uint8_t* row = sm.codes[s] + r * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
-        w[4 * c] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((cc ^ sw) << 4));
+        w[4 * cc] = v.x;
+        w[4 * cc + 1] = v.y;
+        w[4 * cc + 2] = v.z;
+        w[4 * cc + 3] = v.w;
       }
       const uint2 sc = *reinterpret_cast<const uint2*>(sm.scales[s] + r * 8);
       __syncwarp();
@@ -426,58 +531,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.bfull[j]));
-    }
-  } else {
-    // ================= epilogue warps 0 and 1: pages i = e, e + 2, ... (D buffer e);
-    // lane m = query column rq*4 + g of D (TMEM lane 32e + m)
-    const int e = warp, rq = lane >> 2, g = lane & 3;
-    static_assert(kDBufs == 2, "one D buffer per epilogue warp");
-    PageCursor cur = cursor_at(p0 + (e < n ? e : 0), prefix, B);
-    for (int i = e; i < n; i += 2) {
-      const int k = e;
-      alive = wait_bar(smem_u32(&sm.dfull[k]), (i / kDBufs) & 1, p.flags);
-      if (!__all_sync(0xFFFFFFFFu, alive)) {
-        alive = false;
-        break;
-      }
-      tc_fence_after();
-      const int b = cur.b, c = cur.c;
-      const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(b) * p.max_pages + c];
-      const bool page_bad = phys < 0 || phys >= p.num_pages;
-      const int N = ctx_s[b], R = rows_s[b];
-      const bool valid = rq < R && !page_bad;
-      const int t0 = c * kBlock;
-      const int lim = N - R + rq - t0;  // column n of this row is visible iff n <= lim
-      const uint32_t d = tbase + (static_cast<uint32_t>(32 * e) << 16) + k * kDCols;
-      float m = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < kBlock / 32; ++q) {
-        uint32_t v[32];
-        tmem_ld32(d + 32 * q, v);
-        tc_wait_ld();
-        if (MODE == 0) {
-          if (valid) m = fmaxf(m, lim >= kBlock - 1 ? max32(v) : max32_masked(v, 32 * q, lim));
-        } else if (rq < R) {
-          float* out = p.token_scores + (static_cast<long long>(row0_s[b] + rq) * kGroups + g) * p.score_stride + t0;
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int nn = 32 * q + u;
-            if (t0 + nn < N) out[nn] = valid && nn <= lim ? __uint_as_float(v[u]) : -INFINITY;
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
-      if (MODE == 0) {
-        // the group's maximum over its rows: lanes with equal lane % 4
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-        if (lane < kGroups) p.block_S[(static_cast<long long>(b) * kGroups + lane) * p.s_stride + c] = m;
-      }
-      cursor_advance(cur, nb);
-      cursor_advance(cur, nb);
     }
   }
 
@@ -607,10 +660,9 @@ __global__ void dequant_rows_kernel(const uint8_t* codes, const uint8_t* scales,
 }
 
 size_t select_smem_bytes(int num_reqs) {
-  const size_t need = sizeof(Smem) + sizeof(long long) * (num_reqs + 1) + sizeof(int) * (num_reqs + 1) +
-                      3 * sizeof(int) * num_reqs + 1024;
-  // at least 80 KB so no more than two CTAs share an SM's 512 tensor-memory columns
-  return need > 80 * 1024 ? need : 80 * 1024;
+  const size_t need = sizeof(Smem) + sizeof(long long) * (num_reqs + 2) + 1024;
+  // more than half an SM's shared memory, so one CTA holds the SM's 512 tensor-memory columns
+  return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,
