@@ -315,8 +315,8 @@ __device__ __forceinline__ void dq8_signed(uint32_t w, uint32_t L0, uint32_t L1,
 // [vLLM-zh §How; MSA-fig §1 TopK] One warp selects the blocks of one group:
 // the most recent block (nb-1) plus the 15 best of blocks 0..nb-2 by score,
 // ties to the lower id; every block when nb <= 16. ids_out gets 16 ascending
-// ids, -1 padded. S[c] is block c's score (written by this or other CTAs before
-// a device-scope fence; read with plain loads, 16-byte aligned rows).
+// ids, -1 padded. S[c] is block c's score (16-byte aligned rows; plain loads, or
+// with kL2 loads that bypass L1 for scores an earlier kernel wrote).
 //
 // Ranking key: the score's order-preserving integer image in the high word and
 // the complemented block id in the low word, so larger key = higher score, then
@@ -359,8 +359,20 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
   return v;
 }
 
+// Score loads of the top-k: plain loads (scores in shared memory, or written by
+// this CTA), or loads that bypass L1 (scores an earlier kernel wrote).
+template <bool kL2>
+__device__ __forceinline__ float4 topk_ld4(const float* p) {
+  return kL2 ? __ldcg(reinterpret_cast<const float4*>(p)) : *reinterpret_cast<const float4*>(p);
+}
+template <bool kL2>
+__device__ __forceinline__ float topk_ld1(const float* p) {
+  return kL2 ? __ldcg(p) : *p;
+}
+
 // Exact top-(kTopK-1) of nc candidates by insertion into per-lane sorted lists
 // and a 15-round warp merge; the fallback when the threshold filter keeps too many.
+template <bool kL2>
 static __device__ __noinline__ void topk_by_insertion(const float* S, int nc, int32_t* sel) {
   const int lane = threadIdx.x & 31;
   constexpr int L = kTopK - 1;
@@ -368,7 +380,7 @@ static __device__ __noinline__ void topk_by_insertion(const float* S, int nc, in
 #pragma unroll
   for (int j = 0; j < L; ++j) list[j] = 0ull;
   for (int c = lane; c < nc; c += 32) {
-    const uint64_t key = topk_key(S[c], c);
+    const uint64_t key = topk_key(topk_ld1<kL2>(S + c), c);
     if (key > list[L - 1]) {
 #pragma unroll
       for (int j = L - 1; j > 0; --j) list[j] = (key > list[j - 1]) ? list[j - 1] : ((key > list[j]) ? key : list[j]);
@@ -396,6 +408,7 @@ static __device__ __noinline__ void topk_by_insertion(const float* S, int nc, in
 // scratch: 64 u64 per warp (shared memory), for the threshold filter's survivors.
 // S may be global or shared memory (callers stage large score rows in shared
 // memory, where the passes below do not wait on dependent global round trips).
+template <bool kL2 = false>
 static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* ids_out, uint64_t* scratch) {
   const int lane = threadIdx.x & 31;
   if (nb <= kTopK) {
@@ -413,7 +426,7 @@ static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* i
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int c = base + (u * 32 + lane) * 4;
-      v[u] = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = c < nc ? topk_ld4<kL2>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -438,7 +451,7 @@ static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* i
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int c = base + (u * 32 + lane) * 4;
-      v[u] = c < nc ? *reinterpret_cast<const float4*>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[u] = c < nc ? topk_ld4<kL2>(S + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
@@ -457,7 +470,7 @@ static __device__ __noinline__ void warp_topk(const float* S, int nb, int32_t* i
   }
   __syncwarp();
   if (count > 48) {
-    topk_by_insertion(S, nc, sel);
+    topk_by_insertion<kL2>(S, nc, sel);
   } else if (count <= 32) {
     // 4. the survivors, one per lane, sorted descending: the top 15 are lanes 0..14
     const uint64_t k = warp_sort_desc(lane < count ? scratch[lane] : 0ull);
