@@ -180,9 +180,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     sm.soft_dead = 0;
   }
 
-  // block ids are produced by the preceding selection kernel
-  pdl_wait_primary();
-
+  // the request's geometry and query tile are inputs: read them before waiting on the
+  // preceding kernel, which produces the block ids
   const int N = p.context_lens[b];
   const int r0 = p.q_indptr[b], R = p.q_indptr[b + 1] - r0;
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
@@ -193,6 +192,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   }
   if (R == 0) return;
   const int nb = (N + kBlock - 1) / kBlock;
+  const int M = kQPerKV * R;  // query rows of this (request, group): row m = speculative row m/8, head m%8
+  // query tile: 128 rows x 128 bytes, 128-byte swizzle; rows >= M are zero
+  for (int u = tid; u < 128 * 8; u += kAttnThreads) {
+    const int m = u >> 3, ch = u & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v = *reinterpret_cast<const uint4*>(
+          p.q + ((static_cast<long long>(r0 + m / kQPerKV) * kHeads) + kQPerKV * g + m % kQPerKV) * kDim + ch * 16);
+    *reinterpret_cast<uint4*>(sm.qtile + m * 128 + ((ch ^ (m & 7)) << 4)) = v;
+  }
+
+  pdl_wait_primary();  // the block ids come from the selection
+
   if (tid == 0) {
     int n = 0;
     for (int i = 0; i < kTopK; ++i) {
@@ -205,16 +217,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   __syncthreads();
   // the selected blocks' page ids, read once (not on the copy-issue path)
   if (tid < sm.nsel) sm.phys[tid] = p.block_table[static_cast<long long>(b) * p.max_pages + sm.ids[tid]];
-  const int M = kQPerKV * R;  // query rows of this (request, group): row m = speculative row m/8, head m%8
-  // query tile: 128 rows x 128 bytes, 128-byte swizzle; rows >= M are zero
-  for (int u = tid; u < 128 * 8; u += kAttnThreads) {
-    const int m = u >> 3, ch = u & 7;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M)
-      v = *reinterpret_cast<const uint4*>(
-          p.q + ((static_cast<long long>(r0 + m / kQPerKV) * kHeads) + kQPerKV * g + m % kQPerKV) * kDim + ch * 16);
-    *reinterpret_cast<uint4*>(sm.qtile + m * 128 + ((ch ^ (m & 7)) << 4)) = v;
-  }
   fence_proxy_async_smem();
   if (warp == kMmaWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
@@ -569,23 +571,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     }
   }
   __syncthreads();
-  // 2. out[row][4 dims] = sum over splits of weight x partial (16-byte loads, all threads)
-  for (int idx = tid; idx < M * (kDim / 4); idx += kAttnThreads) {
-    const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
-    const long long base = static_cast<long long>(pair) * p.max_m + mrow;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nsplit_used; ++s) {
-      const float w = wgt[mrow * kTopK + s];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (s * stride + base) * kDim) + d4);
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+  // 2. out[row][4 dims] = sum over splits of weight x partial (16-byte loads, all threads);
+  // a thread's loads for 2 items and 2 splits are issued before any is used
+  constexpr int kItems = 2;
+  const int nitems = M * (kDim / 4);
+  for (int idx0 = tid; idx0 < nitems; idx0 += kAttnThreads * kItems) {
+    float4 acc[kItems];
+#pragma unroll
+    for (int t = 0; t < kItems; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit_used; s0 += 2) {
+      float4 v[2][kItems];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int t = 0; t < kItems; ++t) {
+          const int idx = idx0 + t * kAttnThreads, s = s0 + h;
+          const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
+          const long long base = static_cast<long long>(pair) * p.max_m + mrow;
+          v[h][t] = idx < nitems && s < nsplit_used
+                        ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (s * stride + base) * kDim) + d4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int t = 0; t < kItems; ++t) {
+          const int idx = idx0 + t * kAttnThreads, s = s0 + h;
+          if (idx < nitems && s < nsplit_used) {
+            const float w = wgt[(idx / (kDim / 4)) * kTopK + s];
+            acc[t].x += w * v[h][t].x;
+            acc[t].y += w * v[h][t].y;
+            acc[t].z += w * v[h][t].z;
+            acc[t].w += w * v[h][t].w;
+          }
+        }
     }
-    const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
-    const long long orow = (static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh;
-    uint2 packed = make_uint2(bf16x2_bits(acc.x, acc.y), bf16x2_bits(acc.z, acc.w));
-    *reinterpret_cast<uint2*>(p.out + orow * kDim + 4 * d4) = packed;
+#pragma unroll
+    for (int t = 0; t < kItems; ++t) {
+      const int idx = idx0 + t * kAttnThreads;
+      if (idx < nitems) {
+        const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
+        const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
+        const long long orow = (static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh;
+        const uint2 packed = make_uint2(bf16x2_bits(acc[t].x, acc[t].y), bf16x2_bits(acc[t].z, acc[t].w));
+        *reinterpret_cast<uint2*>(p.out + orow * kDim + 4 * d4) = packed;
+      }
+    }
   }
 }
 

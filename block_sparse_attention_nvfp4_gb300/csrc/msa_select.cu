@@ -127,6 +127,17 @@ __device__ __forceinline__ void cursor_advance(PageCursor& pc, const long long* 
   }
 }
 
+// One page forward for a walker that caches its request's page count nbc. Past the
+// last request (b = B) nbc becomes INT_MAX, so the walk never reads beyond prefix[B + 1].
+__device__ __forceinline__ void cursor_step(PageCursor& pc, int& nbc, const long long* prefix, int B) {
+  if (++pc.c >= nbc) {
+    pc.c = 0;
+    do ++pc.b;
+    while (pc.b < B && prefix[pc.b + 1] == prefix[pc.b]);
+    nbc = pc.b < B ? static_cast<int>(prefix[pc.b + 1] - prefix[pc.b]) : INT_MAX;
+  }
+}
+
 // Locate global page index p: request b with prefix[b] <= p < prefix[b+1].
 __device__ __forceinline__ PageCursor cursor_at(long long p, const long long* prefix, int B) {
   int lo = 0, hi = B;  // invariant prefix[lo] <= p < prefix[hi]
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     if (lane == 31) {
       prefix[B] = incl;
-      prefix[B + 1] = incl + (1LL << 40);  // sentinel
+      prefix[B + 1] = incl + (1LL << 30);  // sentinel (a request of 2^30 pages: fits an int)
     }
   }
   __syncthreads();
@@ -392,12 +403,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
       for (int u = 0; u < kIssuers; ++u) {
-        if (++mm.c >= nbc) {  // the next request with pages (the sentinel ends the walk)
-          mm.c = 0;
-          do ++mm.b;
-          while (prefix[mm.b + 1] == prefix[mm.b]);
-          nbc = static_cast<int>(prefix[mm.b + 1] - prefix[mm.b]);
-        }
+        cursor_step(mm, nbc, prefix, B);
       }
       alive = __shfl_sync(0xFFFFFFFFu, alive ? 1 : 0, 0) != 0;  // lane 0 waited and issued
       if (!alive) break;
@@ -485,12 +491,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
       for (int u = 0; u < kPoolSets; ++u) {
-        if (++pc.c >= nbc) {  // the next request with pages (the sentinel ends the walk)
-          pc.c = 0;
-          do ++pc.b;
-          while (prefix[pc.b + 1] == prefix[pc.b]);
-          nbc = static_cast<int>(prefix[pc.b + 1] - prefix[pc.b]);
-        }
+        cursor_step(pc, nbc, prefix, B);
       }
     }
   } else {
