@@ -642,6 +642,91 @@ __device__ __forceinline__ void group_topk(const float* S, int nb, int32_t* ids_
   if (lane < kTopK) ids_out[rank] = my_id;
 }
 
+// group_topk for requests of at most 32 * 4 * 8 + 1 blocks, straight from the scores in
+// global memory (read past L1; no staging): lane l of warp q holds candidates
+// 256 q + 8 l .. + 7 in registers. T = the largest lane maximum with at least 15 lane
+// maxima at or above it, found by rank counting (no sort); the survivors (15 to 19 on the
+// synthetic workloads) are ranked by counting, and the 16 ids ordered the same way. Same
+// result as warp_topk; more than 32 survivors fall back to the exact insertion merge.
+constexpr int kDirectMax = 32 * 4 * 8;  // candidates (blocks but the recent one)
+__device__ __forceinline__ void group_topk_direct(const float* Sg, int nb, int32_t* ids_out, int q, int bar_id,
+                                                  uint64_t* lm, uint64_t* tmax, uint64_t* surv, int* cnt,
+                                                  int32_t* sel) {
+  const int lane = threadIdx.x & 31;
+  constexpr int L = kTopK - 1;
+  const int nc = nb - 1;
+  const int c0 = q * 256 + lane * 8;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 va = c0 < nc ? __ldcg(reinterpret_cast<const float4*>(Sg + c0)) : z;
+  const float4 vb = c0 + 4 < nc ? __ldcg(reinterpret_cast<const float4*>(Sg + c0 + 4)) : z;
+  const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+  uint64_t k[8];
+  uint64_t mx = 0ull;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    k[t] = c0 + t < nc ? topk_key(v[t], c0 + t) : 0ull;
+    mx = k[t] > mx ? k[t] : mx;
+  }
+  lm[q * 32 + lane] = mx;
+  if (q == 0 && lane == 0) *cnt = 0;
+  named_bar_sync(bar_id, 128);
+  int ge = 0;
+#pragma unroll 8
+  for (int j = 0; j < 128; ++j) ge += lm[j] >= mx ? 1 : 0;
+  uint64_t T = ge >= L ? mx : 0ull;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const uint64_t o = shfl_xor_u64(T, off);
+    T = o > T ? o : T;
+  }
+  if (lane == 0) tmax[q] = T;
+  named_bar_sync(bar_id, 128);
+  T = tmax[0];
+#pragma unroll
+  for (int w = 1; w < 4; ++w) T = tmax[w] > T ? tmax[w] : T;
+  // survivors: one atomic per warp reserves the warp's slots
+  int mine = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) mine += (c0 + t < nc && k[t] >= T) ? 1 : 0;
+  int incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int base = 0;
+  if (lane == 31) base = atomicAdd(cnt, incl);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - mine;
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    if (c0 + t < nc && k[t] >= T) {
+      if (base < 64) surv[base] = k[t];
+      ++base;
+    }
+  named_bar_sync(bar_id, 128);
+  if (q != 0) return;
+  const int count = *cnt;
+  if (count > 32) {
+    topk_by_insertion<true>(Sg, nc, sel);
+  } else {
+    const uint64_t key = lane < count ? surv[lane] : 0ull;
+    int rank = 0;
+    for (int j = 0; j < count; ++j) rank += surv[j] > key ? 1 : 0;
+    if (lane < count && rank < L) sel[rank] = topk_id(key);
+    __syncwarp();
+  }
+  // the 15 winners plus the recent block, ascending
+  if (lane == L) sel[L] = nb - 1;
+  __syncwarp();
+  if (lane < kTopK) {
+    const int my_id = sel[lane];
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < kTopK; ++j) rank += sel[j] < my_id ? 1 : 0;
+    ids_out[rank] = my_id;
+  }
+}
+
 // Step 3 of the selection, after the scan: one CTA per request, four warps per group.
 // A kernel of its own so it runs on SMs the scan has left; chained to the scan by
 // programmatic dependent launch, it reads the request geometry before waiting.
@@ -652,6 +737,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p
   __shared__ uint64_t surv[kGroups][64];
   __shared__ int cnt[kGroups];
   __shared__ int32_t sel[kGroups][kTopK];
+  __shared__ uint64_t lm[kGroups][128];
+  __shared__ uint64_t tmax[kGroups][4];
   pdl_launch_dependents();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = warp >> 2, q = warp & 3;
@@ -661,8 +748,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
                   r0 + R <= p.total_rows;
   const int nbb = ok && R > 0 ? (N + kBlock - 1) / kBlock : 0;
+  const bool direct = nbb > kTopK && nbb - 1 <= kDirectMax;  // scores read straight into registers
   pdl_wait_primary();  // the block scores come from the scan kernel
-  if (stage_row > 0 && nbb > 0) {
+  if (stage_row > 0 && nbb > 0 && !direct) {
     // stage the request's 4 score rows, issuing every load of a thread before its stores
     // (one round trip to L2 instead of one per load); loads bypass L1, whose lines may
     // predate the scan
@@ -696,7 +784,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p
       for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = -INFINITY;
     return;
   }
-  if (stage_row > 0) {
+  if (direct) {
+    const float* S = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
+    group_topk_direct(S, nbb, ids, q, 1 + g, lm[g], tmax[g], surv[g], &cnt[g], sel[g]);
+    if (sout != nullptr)
+      for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = c < nbb ? __ldcg(S + c) : -INFINITY;
+  } else if (stage_row > 0) {
     const float* S = tk_stage + g * stage_row;
     group_topk(S, nbb, ids, q, 1 + g, tq[g], surv[g], &cnt[g], sel[g]);
     if (sout != nullptr)
