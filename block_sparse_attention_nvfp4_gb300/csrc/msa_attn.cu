@@ -50,10 +50,11 @@ namespace msa {
 
 namespace {
 
-// Warp w may access TMEM lanes 32 (w % 4) .. + 31; query rows are lanes 0..63.
-constexpr int kSoftWarps = 4;                       // warps 0, 1 (keys / dims 0..63), 4, 5 (64..127)
-constexpr int kMmaWarp = 2;                         // MMA issue, TMEM allocation
-constexpr int kLoadWarp = 3;                        // raw page copies
+// Warp w may access TMEM lanes 32 (w % 4) .. + 31. Query rows are lanes 0..63 and again
+// 64..127; softmax warp q owns lanes 32q .. 32q + 31 (one per SM sub-partition).
+constexpr int kSoftWarps = 4;                       // warps 0..3: keys 0..63 (q < 2) or 64..127
+constexpr int kMmaWarp = 4;                         // MMA issue, TMEM allocation
+constexpr int kLoadWarp = 5;                        // raw page copies
 constexpr int kDqWarp0 = 6, kDqWarps = 8;           // warps 6..13: K rows (0..127), V rows (128..255)
 constexpr int kAttnThreads = (kDqWarp0 + kDqWarps) * 32;
 constexpr int kAttnStages = 2;                      // raw NVFP4 page ring
@@ -81,12 +82,12 @@ struct AttnSmem {
   uint8_t ksc[kAttnStages][kHeadScaleBytes];
   uint8_t vsc[kAttnStages][kHeadScaleBytes];
   uint2 lut[128 * kLutCopies];                      // scaled magnitudes per scale magnitude, interleaved
-  float wgt[64 * kTopK];                            // split-merge weights
-  float xmax[2][64];                                // softmax halves' row maxima / sums
+  float xmax[2][64];                                // key halves' reference maxima and sums
+  float xsum[2][64];
   int soft_dead;                                    // a softmax warp gave up waiting
   uint64_t raw_full[kAttnStages], raw_empty[kAttnStages];
   uint64_t tile_full[kTileBufs], tile_free[kTileBufs];
-  uint64_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs], p_free[kSBufs], o_done;
+  uint64_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs], p_free[kSBufs], o_done, o_final;
   int stage_bad[kAttnStages];
   int ids[kTopK];
   int phys[kTopK];                                  // block-table entries of the selected blocks
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       mbar_init(smem_u32(&sm.p_free[t]), 1);
     }
     mbar_init(smem_u32(&sm.o_done), 1);
+    mbar_init(smem_u32(&sm.o_final), 1);
     mbar_fence_init();
     sm.soft_dead = 0;
   }
@@ -193,13 +195,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   if (R == 0) return;
   const int nb = (N + kBlock - 1) / kBlock;
   const int M = kQPerKV * R;  // query rows of this (request, group): row m = speculative row m/8, head m%8
-  // query tile: 128 rows x 128 bytes, 128-byte swizzle; rows >= M are zero
+  // query tile: 128 rows x 128 bytes, 128-byte swizzle; row 64 + m repeats row m, and
+  // rows m >= M (and 64 + m) are zero
   for (int u = tid; u < 128 * 8; u += kAttnThreads) {
-    const int m = u >> 3, ch = u & 7;
+    const int m = u >> 3, ch = u & 7, mq = m & 63;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M)
+    if (mq < M)
       v = *reinterpret_cast<const uint4*>(
-          p.q + ((static_cast<long long>(r0 + m / kQPerKV) * kHeads) + kQPerKV * g + m % kQPerKV) * kDim + ch * 16);
+          p.q + ((static_cast<long long>(r0 + mq / kQPerKV) * kHeads) + kQPerKV * g + mq % kQPerKV) * kDim + ch * 16);
     *reinterpret_cast<uint4*>(sm.qtile + m * 128 + ((ch ^ (m & 7)) << 4)) = v;
   }
 
@@ -307,7 +310,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA warp: S_j = Q K_j^T and O += P_j V_j, each issued as soon as
-    // its inputs are ready (S_{j+1} does not wait behind P_j V_j or the reverse)
+    // its inputs are ready (S_{j+1} does not wait behind P_j V_j or the reverse), except
+    // that S_j follows P_{j-2} V_{j-2}: both wait for the same softmax arrival, and this
+    // order makes S_j's completion imply that P_{j-2} V_{j-2} is done, which the softmax
+    // warps' waits on o_done and on P buffer j % 2 rely on
     if (lane == 0) {
       const uint64_t qdesc = sdesc_kmajor_sw128(smem_u32(sm.qtile));
       const uint32_t id_qk = idesc_e4m3_f32(128, kBlock, false, false);
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       long long t_last = global_ns();
       while (np < nmy) {
         bool did = false;
-        if (nq < nmy) {
+        if (nq < nmy && np + 1 >= nq) {
           const int tb = nq % kTileBufs, sb = nq % kSBufs;
           if (mbar_test(smem_u32(&sm.tile_full[tb]), (nq / kTileBufs) & 1) &&
               (nq < kSBufs || mbar_test(smem_u32(&sm.s_free[sb]), ((nq / kSBufs) - 1) & 1))) {
@@ -347,6 +353,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
             mma_commit(smem_u32(&sm.tile_free[tb]));
             mma_commit(smem_u32(&sm.p_free[sb]));
             ++np;
+            if (np == nmy) mma_commit(smem_u32(&sm.o_final));  // single phase: O is complete
             did = true;
           }
         }
@@ -361,26 +368,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     }
     __syncwarp();
   } else {
-    // ================= softmax warps: row m = TMEM lane; half hf = keys / dims 64 hf .. 64 hf + 63
-    const int hf = warp >> 2;
-    const int m = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // ================= softmax warps: warp q reads TMEM lanes 32q .. 32q + 31, which hold
+    // query row m = 32 (q & 1) + lane, and takes keys 64 hf .. 64 hf + 63 of every block,
+    // hf = q >> 1. Its lanes' O sums this key half only (the P columns of the other half
+    // stay zero there), with its own reference max and running sum; the two halves of a
+    // row are combined once, at the end.
+    const int q = warp, hf = q >> 1;
+    const int m = 32 * (q & 1) + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     const int rq = m / kQPerKV;
     const int pos_max = N - R + rq;  // this row sees key positions <= pos_max
     const float c = p.sm_scale_log2;
-    float mref = -INFINITY, lrun = 0.f;  // reference max (log2 domain) and this half's running sum
+    float mref = -INFINITY, lrun = 0.f;  // reference max (log2 domain) and running sum
     bool good = true;
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) z[u] = 0u;
+#pragma unroll
+      for (int bb = 0; bb < kSBufs; ++bb) tmem_st32(tbase + lane_base + kColP + 64 * bb + 32 * (hf ^ 1), z);
+      tc_wait_st();
+    }
     for (int j = 0; j < nmy; ++j) {
       const int bb = j % kSBufs;
       const int pos0 = sm.ids[jb0 + j] * kBlock;
       const bool full_vis = pos0 + kBlock - 1 <= N - R;  // every key visible to every row
       const int lim = pos_max - pos0 - 64 * hf;           // key 64 hf + n visible iff n <= lim
-      if (good && !wait_bar(smem_u32(&sm.s_full[bb]), (j / kSBufs) & 1, p.flags)) good = false;
-      good = __all_sync(0xFFFFFFFFu, good);  // warp-uniform from here (collective TMEM loads)
+      good = __all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.s_full[bb]), (j / kSBufs) & 1, p.flags));
+      if (!good) break;
+      tc_fence_after();
       float sv[64];
-      float mx = -INFINITY;
-      if (good) {
-        tc_fence_after();
+      {
         const uint32_t s_addr = tbase + lane_base + kColS + kBlock * bb + 64 * hf;
         uint32_t v0[32], v1[32];
         tmem_ld32(s_addr, v0);
@@ -391,45 +409,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
           sv[u] = __uint_as_float(v0[u]);
           sv[32 + u] = __uint_as_float(v1[u]);
         }
-        if (!full_vis)
-#pragma unroll
-          for (int u = 0; u < 64; ++u) sv[u] = u <= lim ? sv[u] : -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 64; u += 2) mx = fmaxf(mx, fmaxf(sv[u], sv[u + 1]));
       }
-      // the other half's maximum of this row (scores are raw here: c > 0 keeps the order);
-      // the 4 softmax warps pass the same barriers every block, and give up together
-      sm.xmax[hf][m] = mx;
-      if (!good) sm.soft_dead = 1;
-      named_bar_sync(1, kSoftWarps * 32);
-      const float mo = sm.xmax[hf ^ 1][m];
-      const bool dead = sm.soft_dead != 0;
-      named_bar_sync(1, kSoftWarps * 32);  // both halves have read before the next block writes
-      if (dead) {
-        good = false;
-        break;
-      }
+      if (!full_vis)
+#pragma unroll
+        for (int u = 0; u < 64; ++u) sv[u] = u <= lim ? sv[u] : -INFINITY;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 64; u += 2) mx = fmaxf(mx, fmaxf(sv[u], sv[u + 1]));
       // Lazy rescale: P is taken relative to a reference max mref that moves only
       // when this block's max exceeds it by more than kRescaleLog2 (P then stays
       // below 2^kRescaleLog2, well inside FP16); O / l is exact whatever mref is.
-      const float bmax = fmaxf(mx, mo) * c;
+      const float bmax = mx * c;  // c > 0 keeps the order of the raw scores
       const bool move = bmax > mref + kRescaleLog2 || (mref == -INFINITY && bmax != -INFINITY);
       const float m_new = move ? bmax : mref;
       const float ref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = exp2f(mref - ref);  // 0 while nothing was seen yet
       const bool rescale = move && mref != -INFINITY;
       if (j >= 1 && __any_sync(0xFFFFFFFFu, rescale)) {
-        // O must hold every earlier block before it is rescaled
+        // O must hold every earlier block before it is rescaled (S_j's completion already
+        // implies P_{j-2} V_{j-2}, so the phase awaited here is P_{j-1} V_{j-1}'s)
         if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.o_done), (j - 1) & 1, p.flags))) {
-          good = false;  // leaves at the next block's barriers, with the other warps
-          continue;
+          good = false;
+          break;
         }
         tc_fence_after();
         const float a = rescale ? alpha : 1.f;
-#pragma unroll
-        for (int qc = 0; qc < 2; ++qc) {
+#pragma unroll 1
+        for (int qc = 0; qc < 4; ++qc) {  // one 32-column chunk live at a time
           uint32_t v[32];
-          const uint32_t o_addr = tbase + lane_base + kColO + 64 * hf + 32 * qc;
+          const uint32_t o_addr = tbase + lane_base + kColO + 32 * qc;
           tmem_ld32(o_addr, v);
           tc_wait_ld();
 #pragma unroll
@@ -440,11 +448,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         // this P buffer's previous P V (block j - 2) must have finished reading it
         if (!__all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.p_free[bb]), ((j / kSBufs) - 1) & 1, p.flags))) {
           good = false;
-          continue;
+          break;
         }
         tc_fence_after();
       }
-      // P = exp2(s c - max) for this half's 64 keys, FP16 pairs (2 keys per TMEM column)
+      // P = exp2(s c - ref) for this half's 64 keys, FP16 pairs (2 keys per TMEM column)
       uint32_t pw[32];
       uint32_t hsum = 0u;  // f16x2 partial sums
 #pragma unroll
@@ -473,20 +481,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         mbar_arrive(smem_u32(&sm.p_full[bb]));
       }
     }
-    // ---- output: O / l once the last P V has finished (l = both halves' sums)
-    sm.xmax[hf][m] = lrun;
+    // ---- output: row m's two key halves (lanes m and 64 + m, warps q and q ^ 2) combined
+    // with the log-sum-exp rule; warp q writes dims 64 hf .. 64 hf + 63, taking the other
+    // warp's weighted O for those dims through shared memory (the K tiles, free once O is
+    // complete)
+    const bool fin = good && nmy > 0 &&
+                     __all_sync(0xFFFFFFFFu, wait_bar(smem_u32(&sm.o_final), 0, p.flags));
+    sm.xmax[hf][m] = mref;
+    sm.xsum[hf][m] = lrun;
+    if (!fin) sm.soft_dead = 1;
     named_bar_sync(1, kSoftWarps * 32);
-    const float lrow = lrun + sm.xmax[hf ^ 1][m];
-    if (__all_sync(0xFFFFFFFFu, good && nmy > 0 && wait_bar(smem_u32(&sm.o_done), (nmy - 1) & 1, p.flags))) {
+    if (sm.soft_dead == 0) {
       tc_fence_after();
-      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
-      const float lse2 = lrow > 0.f ? mref + log2f(lrow) : -INFINITY;
+      const float mo = sm.xmax[hf ^ 1][m], lo = sm.xsum[hf ^ 1][m];
+      const float mt = fmaxf(mref, mo);
+      const float ref = mt == -INFINITY ? 0.f : mt;
+      const float es = exp2f(mref - ref), eo = exp2f(mo - ref);
+      const float l = lrun * es + lo * eo;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float ws = es * inv;  // weight of this half's O
+      const float lse2 = l > 0.f ? ref + log2f(l) : -INFINITY;
+      static_assert(kSoftWarps * 32 * 64 * sizeof(float) <= 2 * kTileBytes, "exchange fits two K tiles");
+      // lane row of 64 floats, 16-byte chunk ch at slot (ch + lane) % 16: conflict-free
+      float* xrow = reinterpret_cast<float*>(sm.ktile[0]) + (q * 32 + lane) * 64;
+#pragma unroll
+      for (int qc = 0; qc < 2; ++qc) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_base + kColO + 64 * (hf ^ 1) + 32 * qc, v);
+        tc_wait_ld();
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4)
+          *reinterpret_cast<float4*>(xrow + 4 * ((8 * qc + u4 + lane) & 15)) =
+              make_float4(__uint_as_float(v[4 * u4]) * ws, __uint_as_float(v[4 * u4 + 1]) * ws,
+                          __uint_as_float(v[4 * u4 + 2]) * ws, __uint_as_float(v[4 * u4 + 3]) * ws);
+      }
+      named_bar_sync(1, kSoftWarps * 32);
+      const float* xo = reinterpret_cast<const float*>(sm.ktile[0]) + ((q ^ 2) * 32 + lane) * 64;
       const int hh = m % kQPerKV;
 #pragma unroll
       for (int qc = 0; qc < 2; ++qc) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_base + kColO + 64 * hf + 32 * qc, v);
         tc_wait_ld();
+        float o[32];
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4) {
+          const float4 x = *reinterpret_cast<const float4*>(xo + 4 * ((8 * qc + u4 + lane) & 15));
+          o[4 * u4] = fmaf(__uint_as_float(v[4 * u4]), ws, x.x);
+          o[4 * u4 + 1] = fmaf(__uint_as_float(v[4 * u4 + 1]), ws, x.y);
+          o[4 * u4 + 2] = fmaf(__uint_as_float(v[4 * u4 + 2]), ws, x.z);
+          o[4 * u4 + 3] = fmaf(__uint_as_float(v[4 * u4 + 3]), ws, x.w);
+        }
         const int d0 = 64 * hf + 32 * qc;
         if (m < M) {
           if (p.splits == 1) {
@@ -494,19 +539,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
                 p.out + ((static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh) * kDim + d0);
 #pragma unroll
             for (int u8 = 0; u8 < 4; ++u8)
-              out[u8] = make_uint4(
-                  bf16x2_bits(__uint_as_float(v[8 * u8]) * inv, __uint_as_float(v[8 * u8 + 1]) * inv),
-                  bf16x2_bits(__uint_as_float(v[8 * u8 + 2]) * inv, __uint_as_float(v[8 * u8 + 3]) * inv),
-                  bf16x2_bits(__uint_as_float(v[8 * u8 + 4]) * inv, __uint_as_float(v[8 * u8 + 5]) * inv),
-                  bf16x2_bits(__uint_as_float(v[8 * u8 + 6]) * inv, __uint_as_float(v[8 * u8 + 7]) * inv));
+              out[u8] = make_uint4(bf16x2_bits(o[8 * u8], o[8 * u8 + 1]), bf16x2_bits(o[8 * u8 + 2], o[8 * u8 + 3]),
+                                   bf16x2_bits(o[8 * u8 + 4], o[8 * u8 + 5]),
+                                   bf16x2_bits(o[8 * u8 + 6], o[8 * u8 + 7]));
           } else {
             const long long base =
                 (static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m + m;
             float4* po = reinterpret_cast<float4*>(p.part_o + base * kDim + d0);
 #pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4)
-              po[u4] = make_float4(__uint_as_float(v[4 * u4]) * inv, __uint_as_float(v[4 * u4 + 1]) * inv,
-                                   __uint_as_float(v[4 * u4 + 2]) * inv, __uint_as_float(v[4 * u4 + 3]) * inv);
+            for (int u4 = 0; u4 < 8; ++u4) po[u4] = make_float4(o[4 * u4], o[4 * u4 + 1], o[4 * u4 + 2], o[4 * u4 + 3]);
           }
         }
       }
@@ -521,7 +562,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     }
   }
 
-  // ---- teardown
+  // ---- teardown (a CTA that wrote partials makes them visible before it counts itself in)
+  if (p.splits > 1) __threadfence();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -531,8 +573,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
 
   if (p.splits == 1) return;
   // ---- last CTA of this (request, group) merges the splits' partials
-  __threadfence();
-  __syncthreads();
   if (tid == 0) {
     const unsigned old = atomicAdd(p.pair_cnt + pair, 1u);
     sm.last = old + 1 == static_cast<unsigned>(p.splits);
@@ -543,67 +583,49 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
   __threadfence();
   const int nsplit_used = (sm.nsel + p.blocks_per_split - 1) / p.blocks_per_split;
   const long long stride = static_cast<long long>(p.num_reqs) * kGroups * p.max_m;
-  // 1. per query row: the splits' weights exp2(lse2_s - ref) / sum, and the row's lse
-  float* wgt = sm.wgt;  // [M][kTopK]
-  for (int mrow = tid; mrow < M; mrow += kAttnThreads) {
-    const long long base = static_cast<long long>(pair) * p.max_m + mrow;
-    float l2[kTopK];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < kTopK; ++s) {
-      l2[s] = s < nsplit_used ? __ldcg(p.part_lse2 + s * stride + base) : -INFINITY;
-      mx = fmaxf(mx, l2[s]);
-    }
-    const float ref = mx == -INFINITY ? 0.f : mx;
-    float den = 0.f;
-#pragma unroll
-    for (int s = 0; s < kTopK; ++s) {
-      l2[s] = s < nsplit_used ? exp2f(l2[s] - ref) : 0.f;
-      den += l2[s];
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-    for (int s = 0; s < kTopK; ++s) wgt[mrow * kTopK + s] = l2[s] * inv;
-    if (p.lse != nullptr) {
-      const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
-      p.lse[(static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh] =
-          den > 0.f ? (ref + log2f(den)) * 0.69314718055994531f : -INFINITY;
-    }
-  }
-  __syncthreads();
-  // 2. out[row][4 dims] = sum over splits of weight x partial (16-byte loads, all threads);
-  // a thread's loads for 2 items and 2 splits are issued before any is used
-  constexpr int kItems = 2;
+  // out[row][4 dims] = sum over splits s of exp2(lse2_s - lse2) x o_s, lse2 = log2 sum_s exp2(lse2_s),
+  // taken two splits at a time with a running maximum. A thread issues the loads of all its
+  // items (partials and their rows' lse2) before it uses any, so a merge of up to two splits
+  // is one round trip to L2.
+  constexpr int kItems = 5;
   const int nitems = M * (kDim / 4);
   for (int idx0 = tid; idx0 < nitems; idx0 += kAttnThreads * kItems) {
     float4 acc[kItems];
+    float mx[kItems], den[kItems];
 #pragma unroll
-    for (int t = 0; t < kItems; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < kItems; ++t) {
+      acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      mx[t] = -INFINITY;
+      den[t] = 0.f;
+    }
     for (int s0 = 0; s0 < nsplit_used; s0 += 2) {
       float4 v[2][kItems];
+      float l2[2][kItems];
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int t = 0; t < kItems; ++t) {
           const int idx = idx0 + t * kAttnThreads, s = s0 + h;
           const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
-          const long long base = static_cast<long long>(pair) * p.max_m + mrow;
-          v[h][t] = idx < nitems && s < nsplit_used
-                        ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (s * stride + base) * kDim) + d4)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          const long long base = s * stride + static_cast<long long>(pair) * p.max_m + mrow;
+          const bool ok = idx < nitems && s < nsplit_used;
+          v[h][t] = ok ? __ldcg(reinterpret_cast<const float4*>(p.part_o + base * kDim) + d4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          l2[h][t] = ok ? __ldcg(p.part_lse2 + base) : -INFINITY;
         }
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int t = 0; t < kItems; ++t) {
-          const int idx = idx0 + t * kAttnThreads, s = s0 + h;
-          if (idx < nitems && s < nsplit_used) {
-            const float w = wgt[(idx / (kDim / 4)) * kTopK + s];
-            acc[t].x += w * v[h][t].x;
-            acc[t].y += w * v[h][t].y;
-            acc[t].z += w * v[h][t].z;
-            acc[t].w += w * v[h][t].w;
-          }
+          const float nm = fmaxf(mx[t], l2[h][t]);
+          const float ref = nm == -INFINITY ? 0.f : nm;
+          const float a = exp2f(mx[t] - ref), w = exp2f(l2[h][t] - ref);
+          acc[t].x = acc[t].x * a + w * v[h][t].x;
+          acc[t].y = acc[t].y * a + w * v[h][t].y;
+          acc[t].z = acc[t].z * a + w * v[h][t].z;
+          acc[t].w = acc[t].w * a + w * v[h][t].w;
+          den[t] = den[t] * a + w;
+          mx[t] = nm;
         }
     }
 #pragma unroll
@@ -613,8 +635,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         const int mrow = idx / (kDim / 4), d4 = idx % (kDim / 4);
         const int rq = mrow / kQPerKV, hh = mrow % kQPerKV;
         const long long orow = (static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh;
-        const uint2 packed = make_uint2(bf16x2_bits(acc[t].x, acc[t].y), bf16x2_bits(acc[t].z, acc[t].w));
+        const float inv = den[t] > 0.f ? 1.f / den[t] : 0.f;
+        const uint2 packed = make_uint2(bf16x2_bits(acc[t].x * inv, acc[t].y * inv),
+                                        bf16x2_bits(acc[t].z * inv, acc[t].w * inv));
         *reinterpret_cast<uint2*>(p.out + orow * kDim + 4 * d4) = packed;
+        if (d4 == 0 && p.lse != nullptr)
+          p.lse[orow] = den[t] > 0.f ? (mx[t] + log2f(den[t])) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
