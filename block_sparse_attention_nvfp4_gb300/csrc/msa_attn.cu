@@ -86,7 +86,7 @@ struct AttnSmem {
   float xsum[2][64];
   int soft_dead;                                    // a softmax warp gave up waiting
   uint64_t raw_full[kAttnStages], raw_empty[kAttnStages];
-  uint64_t tile_full[kTileBufs], tile_free[kTileBufs];
+  uint64_t ktile_full[kTileBufs], vtile_full[kTileBufs], tile_free[kTileBufs];
   uint64_t s_full[kSBufs], s_free[kSBufs], p_full[kSBufs], p_free[kSBufs], o_done, o_final;
   int stage_bad[kAttnStages];
   int ids[kTopK];
@@ -167,7 +167,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       mbar_init(smem_u32(&sm.raw_empty[s]), kDqWarps);
     }
     for (int t = 0; t < kTileBufs; ++t) {
-      mbar_init(smem_u32(&sm.tile_full[t]), kDqWarps);
+      mbar_init(smem_u32(&sm.ktile_full[t]), kDqWarps / 2);  // the K-row warps
+      mbar_init(smem_u32(&sm.vtile_full[t]), kDqWarps / 2);  // the V-row warps
       mbar_init(smem_u32(&sm.tile_free[t]), 1);
     }
     for (int t = 0; t < kSBufs; ++t) {
@@ -260,9 +261,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     }
     __syncwarp();
   } else if (warp >= kDqWarp0) {
-    // ================= dequant warps: thread t = K row t (t < 128) or V row t - 128
+    // ================= dequant warps: thread t = row t & 127 of K or of V. A V row costs
+    // about twice a K row (its E4M3 values are widened to FP16), so the two halves of the
+    // warps swap K and V every block: a half that finishes block j's K rows early goes on
+    // to block j + 1's V rows
     const int t = tid - kDqWarp0 * 32;
-    const bool is_v = t >= kBlock;
     const int r = t & (kBlock - 1), r7 = r & 7;
     // chunk order k = c ^ h((r >> 1) & 3), h = multiplication by a generator of GF(4)
     // (0,1,2,3 -> 0,2,3,1): both h and x ^ h(x) are permutations, so the 8 rows of a
@@ -273,24 +276,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     for (int j = 0; j < nmy; ++j) {
       const int st = j % kAttnStages, buf = j % kTileBufs;
       if (!wait_bar(smem_u32(&sm.raw_full[st]), (j / kAttnStages) & 1, p.flags)) break;
+      const bool is_v = (t >= kBlock) != ((j & 1) != 0);
+      // the row's codes and scales go to registers and the stage back to the load warp at
+      // once, so the copy of block j + kAttnStages overlaps this block's dequantisation
+      const bool bad = sm.stage_bad[st] != 0;
+      const uint8_t* row = (is_v ? sm.vc[st] : sm.kc[st]) + r * 64;
+      const uint2 sc = *reinterpret_cast<const uint2*>((is_v ? sm.vsc[st] : sm.ksc[st]) + r * 8);
+      uint4 v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(row + ((c ^ h) << 4));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.raw_empty[st]));
       if (j >= kTileBufs && !wait_bar(smem_u32(&sm.tile_free[buf]), ((j / kTileBufs) - 1) & 1, p.flags)) break;
       const int pos0 = sm.ids[jb0 + j] * kBlock;
       const int nvalid = N - pos0 < kBlock ? N - pos0 : kBlock;
       const uint32_t row_addr = smem_u32(is_v ? sm.vtile[buf][0] : sm.ktile[buf]) + static_cast<uint32_t>(r) * 128u;
       // a bad page reads as zeros; V rows past the context are zero (their weights are
       // 0, and 0 x NaN from unwritten slots must not reach P V)
-      if (sm.stage_bad[st] != 0 || (is_v && r >= nvalid)) {
+      if (bad || (is_v && r >= nvalid)) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + (c << 4), 0u, 0u, 0u, 0u);
         if (is_v)
 #pragma unroll
           for (int c = 0; c < 8; ++c) st_shared_v4(row_addr + kVHalfBytes + (c << 4), 0u, 0u, 0u, 0u);
       } else {
-        const uint8_t* row = (is_v ? sm.vc[st] : sm.kc[st]) + r * 64;
-        const uint2 sc = *reinterpret_cast<const uint2*>((is_v ? sm.vsc[st] : sm.ksc[st]) + r * 8);
-        uint4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(row + ((c ^ h) << 4));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int k = c ^ h;
@@ -303,10 +312,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       }
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sm.tile_full[buf]));
-        mbar_arrive(smem_u32(&sm.raw_empty[st]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(is_v ? &sm.vtile_full[buf] : &sm.ktile_full[buf]));
     }
   } else if (warp == kMmaWarp) {
     // ================= MMA warp: S_j = Q K_j^T and O += P_j V_j, each issued as soon as
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         bool did = false;
         if (nq < nmy && np + 1 >= nq) {
           const int tb = nq % kTileBufs, sb = nq % kSBufs;
-          if (mbar_test(smem_u32(&sm.tile_full[tb]), (nq / kTileBufs) & 1) &&
+          if (mbar_test(smem_u32(&sm.ktile_full[tb]), (nq / kTileBufs) & 1) &&
               (nq < kSBufs || mbar_test(smem_u32(&sm.s_free[sb]), ((nq / kSBufs) - 1) & 1))) {
             tc_fence_after();
             // K step kk of an operand: +32 bytes along K-major rows (+2 in the address field)
@@ -339,7 +345,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
         }
         if (np < nq) {
           const int tb = np % kTileBufs, sb = np % kSBufs;
-          if (mbar_test(smem_u32(&sm.p_full[sb]), (np / kSBufs) & 1)) {
+          if (mbar_test(smem_u32(&sm.p_full[sb]), (np / kSBufs) & 1) &&
+              mbar_test(smem_u32(&sm.vtile_full[tb]), (np / kTileBufs) & 1)) {
             tc_fence_after();
             // MN-major V: 128 dims = two 128-byte swizzle atoms (the two halves, kVHalfBytes
             // apart: the leading-dimension offset), 8-key groups 1 KB apart (the stride
