@@ -525,6 +525,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
       named_bar_sync(1, kSoftWarps * 32);
       const float* xo = reinterpret_cast<const float*>(sm.ktile[0]) + ((q ^ 2) * 32 + lane) * 64;
       const int hh = m % kQPerKV;
+      // the finished O rows (FP32), staged in the V tiles (free once O is complete)
+      static_assert(64 * kDim * sizeof(float) <= 2 * kVHalfBytes, "staging fits one V tile buffer");
+      float* stage = reinterpret_cast<float*>(sm.vtile[0][0]);
 #pragma unroll
       for (int qc = 0; qc < 2; ++qc) {
         uint32_t v[32];
@@ -539,23 +542,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
           o[4 * u4 + 2] = fmaf(__uint_as_float(v[4 * u4 + 2]), ws, x.z);
           o[4 * u4 + 3] = fmaf(__uint_as_float(v[4 * u4 + 3]), ws, x.w);
         }
-        const int d0 = 64 * hf + 32 * qc;
-        if (m < M) {
-          if (p.splits == 1) {
-            uint4* out = reinterpret_cast<uint4*>(
-                p.out + ((static_cast<long long>(r0 + rq) * kHeads) + kQPerKV * g + hh) * kDim + d0);
+        // combined row m, dims 64 hf + 32 qc .. + 31 (16-byte chunks 16 hf + 8 qc + u4) into the
+        // staging rows; chunk c of row m sits at c ^ (m & 7), so 8 rows hit 8 bank groups
 #pragma unroll
-            for (int u8 = 0; u8 < 4; ++u8)
-              out[u8] = make_uint4(bf16x2_bits(o[8 * u8], o[8 * u8 + 1]), bf16x2_bits(o[8 * u8 + 2], o[8 * u8 + 3]),
-                                   bf16x2_bits(o[8 * u8 + 4], o[8 * u8 + 5]),
-                                   bf16x2_bits(o[8 * u8 + 6], o[8 * u8 + 7]));
-          } else {
-            const long long base =
-                (static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m + m;
-            float4* po = reinterpret_cast<float4*>(p.part_o + base * kDim + d0);
-#pragma unroll
-            for (int u4 = 0; u4 < 8; ++u4) po[u4] = make_float4(o[4 * u4], o[4 * u4 + 1], o[4 * u4 + 2], o[4 * u4 + 3]);
-          }
+        for (int u4 = 0; u4 < 8; ++u4)
+          *reinterpret_cast<float4*>(stage + m * kDim + 4 * ((16 * hf + 8 * qc + u4) ^ (m & 7))) =
+              make_float4(o[4 * u4], o[4 * u4 + 1], o[4 * u4 + 2], o[4 * u4 + 3]);
+      }
+      named_bar_sync(1, kSoftWarps * 32);
+      // coalesced copy-out by the 128 softmax threads: consecutive threads, consecutive
+      // 16-byte pieces of an output row
+      const int ct = q * 32 + lane;
+      if (p.splits == 1) {
+        for (int it = ct; it < M * (kDim / 8); it += kSoftWarps * 32) {
+          const int mm = it / (kDim / 8), c8 = it % (kDim / 8);  // 8 dims: chunks 2 c8, 2 c8 + 1
+          const float4 a = *reinterpret_cast<const float4*>(stage + mm * kDim + 4 * ((2 * c8) ^ (mm & 7)));
+          const float4 b = *reinterpret_cast<const float4*>(stage + mm * kDim + 4 * ((2 * c8 + 1) ^ (mm & 7)));
+          const long long orow = (static_cast<long long>(r0 + mm / kQPerKV) * kHeads) + kQPerKV * g + mm % kQPerKV;
+          *reinterpret_cast<uint4*>(p.out + orow * kDim + 8 * c8) =
+              make_uint4(bf16x2_bits(a.x, a.y), bf16x2_bits(a.z, a.w), bf16x2_bits(b.x, b.y), bf16x2_bits(b.z, b.w));
+        }
+      } else {
+        const long long base = (static_cast<long long>(blockIdx.x) * p.num_reqs * kGroups + pair) * p.max_m;
+        for (int it = ct; it < M * (kDim / 4); it += kSoftWarps * 32) {
+          const int mm = it / (kDim / 4), c = it % (kDim / 4);
+          *reinterpret_cast<float4*>(p.part_o + (base + mm) * kDim + 4 * c) =
+              *reinterpret_cast<const float4*>(stage + mm * kDim + 4 * (c ^ (mm & 7)));
         }
       }
       if (m < M && hf == 0) {
