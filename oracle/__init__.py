@@ -76,6 +76,14 @@ def _load():
             lib.oracle_attend.argtypes = [ap, ctypes.c_int, ip, dp, dp]
             lib.oracle_decode.argtypes = [ap, ctypes.c_int, ip, ip, dp, dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            fp = ctypes.POINTER(ctypes.c_float)
+            lib.oracle_e2m1_round.restype = ctypes.c_int
+            lib.oracle_e2m1_round.argtypes = [ctypes.c_double]
+            lib.oracle_nvfp4_quantize_row.argtypes = [fp, ctypes.c_int, u8p, u8p]
+            lib.oracle_kv_insert.restype = ctypes.c_int
+            lib.oracle_kv_insert.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int64), fp, fp, fp,
+                                             u8p, u8p, u8p, u8p, u8p, u8p]
             for f in ("oracle_token_scores", "oracle_block_maxpool", "oracle_block_scores", "oracle_select",
                       "oracle_attend", "oracle_decode"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -225,3 +233,56 @@ def decode(wl, reqs=None):
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+# ---------------------------------------------------------------- NVFP4 insertion
+# [vLLM-zh] "QKV GEMM + norm + RoPE + KV insert fusion": new K, V and index keys
+# arrive as FP32 and are quantised to NVFP4 into their caches.
+
+def e2m1_round(y: float) -> int:
+    """E2M1 code (sign in bit 3) of the magnitude nearest |y|, ties to even, saturating."""
+    return int(_load().oracle_e2m1_round(float(y)))
+
+
+def nvfp4_quantize_rows(x: np.ndarray):
+    """FP32 rows [..., n] (n a multiple of 16) -> (codes [..., n/2] u8, scales [..., n/16] u8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n = x.shape[-1]
+    if n % 16:
+        raise ValueError("row length must be a multiple of 16")
+    flat = x.reshape(-1, n)
+    codes = np.zeros((flat.shape[0], n // 2), np.uint8)
+    scales = np.zeros((flat.shape[0], n // 16), np.uint8)
+    lib = _load()
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    fp = ctypes.POINTER(ctypes.c_float)
+    for i in range(flat.shape[0]):
+        lib.oracle_nvfp4_quantize_row(flat[i].ctypes.data_as(fp), n, codes[i].ctypes.data_as(u8p),
+                                      scales[i].ctypes.data_as(u8p))
+    return codes.reshape(x.shape[:-1] + (n // 2,)), scales.reshape(x.shape[:-1] + (n // 16,))
+
+
+def kv_insert(slot_mapping, k, v, ki, caches: dict, num_pages: int) -> int:
+    """Quantise T new tokens into ``caches`` (numpy u8 arrays k_data, k_scale, v_data,
+    v_scale, ki_data, ki_scale, updated in place). k, v: [T][4][128] FP32 or None;
+    ki: [T][128] FP32 or None. Returns the oracle status (0, or -1 for a page out of range)."""
+    lib = _load()
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T = sm.shape[0]
+    fp = ctypes.POINTER(ctypes.c_float)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+
+    def f(a):
+        if a is None:
+            return None, None
+        a = np.ascontiguousarray(a, dtype=np.float32)
+        return a, a.ctypes.data_as(fp)
+
+    (ka, kp), (va, vp), (ia, ip_) = f(k), f(v), f(ki)
+    for name in ("k_data", "k_scale", "v_data", "v_scale", "ki_data", "ki_scale"):
+        if not (caches[name].flags.c_contiguous and caches[name].dtype == np.uint8):
+            raise ValueError(name + " must be a contiguous uint8 array")
+    ptr = {n: caches[n].ctypes.data_as(u8p) for n in caches}
+    return int(lib.oracle_kv_insert(T, num_pages, sm.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), kp, vp, ip_,
+                                    ptr["k_data"], ptr["k_scale"], ptr["v_data"], ptr["v_scale"], ptr["ki_data"],
+                                    ptr["ki_scale"]))

@@ -366,6 +366,77 @@ int oracle_decode(const oracle_args* a, int nreq, const int32_t* reqs, int32_t* 
   return err;
 }
 
+/* ------------------------------------------------------------------------- */
+/* NVFP4 insertion of new keys and values. [vLLM-zh] "QKV GEMM + norm + RoPE + KV */
+/* 插入融合": the fused epilogue takes the FP32 accumulators head by head and     */
+/* quantises K, V and the index keys to NVFP4, writing them straight into their   */
+/* caches. NVFP4 as everywhere here: per 16 consecutive elements one E4M3 scale,  */
+/* amax / 6 rounded to E4M3 (nearest, ties to even, saturating; no second-level   */
+/* scale), and per element the E2M1 value nearest x / scale (ties to the even     */
+/* code, saturating at 6) with the sign of x. A zero scale gives zero codes.      */
+/* ------------------------------------------------------------------------- */
+
+/* E2M1 code of y: sign of y in bit 3, magnitude = the nearest of the 8 E2M1
+ * magnitudes (codes 0..7 in increasing value), ties to the even code, values
+ * beyond 6 saturating to 6. Plain search over the 8 magnitudes. */
+int oracle_e2m1_round(double y) {
+  int sign = signbit(y) ? 8 : 0, c, best = 0;
+  double a = fabs(y), dbest = INFINITY;
+  /* beyond the largest magnitude that magnitude is the nearest (and the distances
+   * to the others can round to equal doubles for huge y) */
+  if (a >= 6.0) return sign | 7;
+  for (c = 0; c < 8; c++) {
+    double d = fabs(oracle_e2m1_value(c) - a);
+    if (d < dbest || (d == dbest && (c & 1) == 0)) { dbest = d; best = c; }
+  }
+  return sign | best;
+}
+
+/* One row of n elements (n a multiple of 16) to n/2 code bytes (element 2i in
+ * the low nibble of byte i) and n/16 scale bytes. */
+void oracle_nvfp4_quantize_row(const float* x, int n, uint8_t* codes, uint8_t* scales) {
+  int g, j;
+  for (g = 0; g < n / 16; g++) {
+    double amax = 0.0, s;
+    for (j = 0; j < 16; j++) amax = fmax(amax, fabs((double)x[g * 16 + j]));
+    scales[g] = (uint8_t)oracle_e4m3_round(amax / 6.0);
+    s = oracle_e4m3_value(scales[g]);
+    for (j = 0; j < 16; j += 2) {
+      int lo = s > 0.0 ? oracle_e2m1_round((double)x[g * 16 + j] / s) : 0;
+      int hi = s > 0.0 ? oracle_e2m1_round((double)x[g * 16 + j + 1] / s) : 0;
+      codes[(g * 16 + j) / 2] = (uint8_t)(lo | (hi << 4));
+    }
+  }
+}
+
+/* Write T new tokens into the caches (layout as in the header): token t goes to
+ * page slot_mapping[t] / 128, slot slot_mapping[t] % 128, as 4 K rows, 4 V rows
+ * and 1 index-key row; a negative slot skips the token, and a NULL source leaves
+ * that cache untouched. Returns OR_EINVAL (after writing the valid tokens) if a
+ * page is out of range. */
+int oracle_kv_insert(int T, int num_pages, const int64_t* slot_mapping, const float* k, const float* v,
+                     const float* ki, uint8_t* k_data, uint8_t* k_scale, uint8_t* v_data, uint8_t* v_scale,
+                     uint8_t* ki_data, uint8_t* ki_scale) {
+  int t, h, err = OR_OK;
+  for (t = 0; t < T; t++) {
+    int64_t sl = slot_mapping[t], page, slot;
+    if (sl < 0) continue;
+    page = sl / OR_BLK;
+    slot = sl % OR_BLK;
+    if (page >= num_pages) { err = OR_EINVAL; continue; }
+    for (h = 0; h < OR_G; h++) {
+      int64_t row = (page * OR_G + h) * OR_BLK + slot;
+      if (k) oracle_nvfp4_quantize_row(k + ((int64_t)t * OR_G + h) * OR_D, OR_D, k_data + row * 64, k_scale + row * 8);
+      if (v) oracle_nvfp4_quantize_row(v + ((int64_t)t * OR_G + h) * OR_D, OR_D, v_data + row * 64, v_scale + row * 8);
+    }
+    if (ki) {
+      int64_t row = page * OR_BLK + slot;
+      oracle_nvfp4_quantize_row(ki + (int64_t)t * OR_D, OR_D, ki_data + row * 64, ki_scale + row * 8);
+    }
+  }
+  return err;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
