@@ -173,6 +173,45 @@ def workload_config(name, spec, l2_note):
 
 
 # ----------------------------------------------------------------------------- libmsa arm
+def measure_kv_insert(l2_flush, stream, reps: int, tokens: int = 131072, pages: int = 1024):
+    """The KV-insert step (msa_kv_insert_nvfp4) alone: `tokens` new tokens (a 128K-token
+    prefill) quantised into `pages` pages through shuffled slots, inputs resident on the
+    device (seeded normal FP32 K, V, index keys), L2 flushed before each launch. HBM-bound:
+    algorithmic bytes per token = 9 rows x (512 B read + 72 B written) + the 8-byte slot."""
+    import torch
+
+    from block_sparse_attention_nvfp4_gb300 import KVCache, _lib
+
+    g = torch.Generator(device="cuda").manual_seed(5)
+    k = torch.randn(tokens, 4, 128, device="cuda", generator=g)
+    v = torch.randn(tokens, 4, 128, device="cuda", generator=g)
+    ki = torch.randn(tokens, 128, device="cuda", generator=g)
+    slots = torch.randperm(pages * 128, device="cuda", generator=g)[:tokens].to(torch.int64)
+    cache = KVCache.empty(pages)
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        cache.insert(slots, k, v, ki, ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        l2_flush()
+        ev[i][0].record(stream)
+        cache.insert(slots, k, v, ki, ws)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    flags = _lib.msa_get_error(ws)
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    nbytes = tokens * (9 * (512 + 72) + 8)
+    peak, peak_kind = measured_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    out = {"tokens": tokens, "rows": 9 * tokens, "us": round(us, 2), "algorithmic_bytes": nbytes,
+           "achieved_gbs": round(gbs, 1), "peak_gbs": peak, "peak_source": peak_kind, "frac": round(gbs / peak, 4),
+           "tokens_per_s": round(tokens / (us * 1e-6), 1), "launches": reps, "device_error_flags": flags,
+           "data": "synthetic: seeded N(0,1) FP32 rows on the device, shuffled slots"}
+    del k, v, ki, cache
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_libmsa(args, rank, world, dist):
     import torch
 
@@ -253,6 +292,8 @@ def run_libmsa(args, rank, world, dist):
     torch.cuda.synchronize()
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in eva)
 
+    kv_insert = measure_kv_insert(l2_flush, stream, reps=min(args.steps, 50))
+
     sel_bytes = bm.select_bytes(wl.context_lens, np.diff(wl.q_indptr))
     step_bytes = bm.step_bytes(wl.context_lens, np.diff(wl.q_indptr), ids_now.cpu().numpy())
     peak, peak_kind = measured_peaks()
@@ -315,6 +356,7 @@ def run_libmsa(args, rank, world, dist):
             "gpu_launches": 3 * args.steps,  # per step: index scan, top-k, sparse attention
             "kernels_us": {"decode": round(ms_per_step * 1e3, 2), "select": round(sel_ms * 1e3, 2),
                            "sparse_attention": round(attn_ms * 1e3, 2)},
+            "kv_insert_nvfp4": kv_insert,
             "clocks": clocks, "timed_wall_s": round(wall, 4), "device_error_flags": ok_flags,
             "impl": "libmsa"}
     return line

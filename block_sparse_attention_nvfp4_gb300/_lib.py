@@ -20,12 +20,12 @@ LIB_PATH = os.path.join(_HERE, "libmsa.so")
 MSA_OK = 0
 STATUS = {0: "MSA_OK", -1: "MSA_ERR_INVALID_ARG", -2: "MSA_ERR_UNSUPPORTED", -3: "MSA_ERR_CUDA",
           -4: "MSA_ERR_WORKSPACE", -5: "MSA_ERR_BAD_TABLE", -6: "MSA_ERR_TIMEOUT"}
-FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS = 0x1, 0x2, 0x4, 0x8
+FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS, FLAG_BAD_SLOT = 0x1, 0x2, 0x4, 0x8, 0x10
 
 # symbols include/msa.h declares (checked by the CPU tests)
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
-           "msa_decode", "msa_dequant_rows")
+           "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4")
 
 
 class MSAError(RuntimeError):
@@ -42,6 +42,15 @@ class Args(ctypes.Structure):
                 ("block_size", ctypes.c_int32), ("top_k", ctypes.c_int32), ("sm_scale", ctypes.c_float),
                 ("context_lens", ctypes.c_void_p), ("q_indptr", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
                 ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
+                ("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("ki_data", ctypes.c_void_p), ("ki_scale", ctypes.c_void_p)]
+
+
+class KvInsertArgs(ctypes.Structure):
+    """Mirror of msa_kv_insert_args."""
+    _fields_ = [("num_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("slot_mapping", ctypes.c_void_p),
+                ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_idx", ctypes.c_void_p),
                 ("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("ki_data", ctypes.c_void_p), ("ki_scale", ctypes.c_void_p)]
@@ -74,6 +83,7 @@ def load(path: str = LIB_PATH):
             lib.msa_sparse_attn_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_dequant_rows.argtypes = [vp, vp, i64, vp, ctypes.c_int32, vp]
+            lib.msa_kv_insert_nvfp4.argtypes = [ctypes.POINTER(KvInsertArgs), vp, sz, vp]
             for f in EXPORTS[1:]:
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -179,3 +189,24 @@ def msa_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Opti
 def msa_dequant_rows(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, path: int, stream=None):
     _check(load().msa_dequant_rows(_ptr(codes), _ptr(scales), codes.shape[0], _ptr(out), int(path),
                                    _stream(stream)), "msa_dequant_rows")
+
+
+def make_kv_insert_args(cache, slot_mapping: torch.Tensor, k: Optional[torch.Tensor], v: Optional[torch.Tensor],
+                        k_idx: Optional[torch.Tensor]) -> KvInsertArgs:
+    """msa_kv_insert_args for T new tokens: slot_mapping int64 [T]; k, v FP32 [T, 4, 128]; k_idx FP32
+    [T, 128] (any may be None); cache as api.KVCache."""
+    a = KvInsertArgs()
+    a.num_tokens = int(slot_mapping.shape[0])
+    a.num_pages = int(cache.num_pages)
+    a.slot_mapping = _ptr(slot_mapping).value
+    for name, t in (("k", k), ("v", v), ("k_idx", k_idx)):
+        p = _ptr(t)
+        setattr(a, name, p.value if p is not None else None)
+    for name in ("k_data", "k_scale", "v_data", "v_scale", "ki_data", "ki_scale"):
+        setattr(a, name, _ptr(getattr(cache, name)).value)
+    return a
+
+
+def msa_kv_insert_nvfp4(args: KvInsertArgs, ws: torch.Tensor, stream=None):
+    _check(load().msa_kv_insert_nvfp4(ctypes.byref(args), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "msa_kv_insert_nvfp4")

@@ -31,6 +31,20 @@ class KVCache:
         t = lambda a: torch.from_numpy(a).to(device)  # noqa: E731
         return KVCache(t(wl.k_data), t(wl.k_scale), t(wl.v_data), t(wl.v_scale), t(wl.ki_data), t(wl.ki_scale))
 
+    @staticmethod
+    def empty(num_pages: int, device="cuda") -> "KVCache":
+        z = lambda *shape: torch.zeros(shape, dtype=torch.uint8, device=device)  # noqa: E731
+        return KVCache(z(num_pages, 4, 128, 64), z(num_pages, 4, 128, 8), z(num_pages, 4, 128, 64),
+                       z(num_pages, 4, 128, 8), z(num_pages, 128, 64), z(num_pages, 128, 8))
+
+    def insert(self, slot_mapping: torch.Tensor, k: Optional[torch.Tensor], v: Optional[torch.Tensor],
+               k_idx: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+        """Quantise T new tokens to NVFP4 into their slots (msa_kv_insert_nvfp4): slot_mapping
+        int64 [T] (page * 128 + slot, negative = skip), k and v FP32 [T, 4, 128], k_idx FP32
+        [T, 128], any of them None; ws a zero-filled workspace of >= 256 bytes (error flags)."""
+        args = _lib.make_kv_insert_args(self, slot_mapping, k, v, k_idx)
+        _lib.msa_kv_insert_nvfp4(args, ws, stream)
+
 
 @dataclasses.dataclass
 class DecodeBatch:

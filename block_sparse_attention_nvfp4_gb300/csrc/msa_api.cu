@@ -384,4 +384,35 @@ msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t
              : MSA_ERR_CUDA;
 }
 
+msa_status msa_kv_insert_nvfp4(const msa_kv_insert_args* a, void* ws, size_t ws_bytes, void* stream) {
+  if (a == nullptr || a->num_tokens < 0 || a->num_pages <= 0) return MSA_ERR_INVALID_ARG;
+  if (a->num_tokens > 0 && a->slot_mapping == nullptr) return MSA_ERR_INVALID_ARG;
+  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if ((a->k != nullptr && (a->k_data == nullptr || a->k_scale == nullptr || misaligned(a->k))) ||
+      (a->v != nullptr && (a->v_data == nullptr || a->v_scale == nullptr || misaligned(a->v))) ||
+      (a->k_idx != nullptr && (a->ki_data == nullptr || a->ki_scale == nullptr || misaligned(a->k_idx))))
+    return MSA_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0 || ws_bytes < kWsAlign)
+    return MSA_ERR_WORKSPACE;
+  DeviceInfo d;
+  msa_status s = check_device(&d);
+  if (s != MSA_OK) return s;
+  if (a->num_tokens == 0 || (a->k == nullptr && a->v == nullptr && a->k_idx == nullptr)) return MSA_OK;
+  KvInsertParams p;
+  p.num_tokens = a->num_tokens;
+  p.num_pages = a->num_pages;
+  p.slot_mapping = a->slot_mapping;
+  p.k = a->k;
+  p.v = a->v;
+  p.ki = a->k_idx;
+  p.k_data = a->k_data;
+  p.k_scale = a->k_scale;
+  p.v_data = a->v_data;
+  p.v_scale = a->v_scale;
+  p.ki_data = a->ki_data;
+  p.ki_scale = a->ki_scale;
+  p.flags = static_cast<uint32_t*>(ws);
+  return launch_kv_insert(p, d.sm_count, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
 }  // extern "C"

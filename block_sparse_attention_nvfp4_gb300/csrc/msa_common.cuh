@@ -31,6 +31,7 @@ constexpr uint32_t kFlagBadPage = 0x1u;
 constexpr uint32_t kFlagBadLength = 0x2u;
 constexpr uint32_t kFlagTimeout = 0x4u;
 constexpr uint32_t kFlagBadIds = 0x8u;
+constexpr uint32_t kFlagBadSlot = 0x10u;
 
 // bounded waits give up after this long (ns of %globaltimer)
 constexpr long long kWaitLimitNs = 1000000000LL;

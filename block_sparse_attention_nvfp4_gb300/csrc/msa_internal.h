@@ -62,6 +62,23 @@ struct AttnParams {
   float* lse;                // optional [rows][32]
 };
 
+// NVFP4 insertion of new tokens (msa_kv_insert_nvfp4).
+struct KvInsertParams {
+  long long num_tokens;
+  int num_pages;
+  const int64_t* slot_mapping;
+  const float* k;
+  const float* v;
+  const float* ki;
+  uint8_t* k_data;
+  uint8_t* k_scale;
+  uint8_t* v_data;
+  uint8_t* v_scale;
+  uint8_t* ki_data;
+  uint8_t* ki_scale;
+  uint32_t* flags;
+};
+
 // Workspace layout, offsets in bytes (each 256-aligned).
 struct WsLayout {
   size_t flags, pair_cnt, block_S, part_o, part_lse2, total;
@@ -86,6 +103,7 @@ cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, in
 cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st);
 cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
 cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
+cudaError_t launch_kv_insert(const KvInsertParams& prm, int sm_count, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,
                                 cudaStream_t st);
 

@@ -86,6 +86,7 @@ typedef enum {
 #define MSA_FLAG_BAD_LENGTH  0x2u   /* context_lens / q_indptr inconsistent with the limits */
 #define MSA_FLAG_TIMEOUT     0x4u   /* an mbarrier / async-copy wait hit its time limit */
 #define MSA_FLAG_BAD_IDS     0x8u   /* msa_sparse_attn_decode got a block id outside the context */
+#define MSA_FLAG_BAD_SLOT    0x10u  /* msa_kv_insert_nvfp4 got a slot on a page outside [0, num_pages) */
 
 typedef struct {
   int32_t num_reqs;            /* B >= 0 */
@@ -193,6 +194,47 @@ msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t*
  * [vLLM-zh, Blackwell kernels: NVFP4 turned into FP8 before the FP8 MMA] */
 msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t nrows,
                             uint8_t* out_e4m3, int32_t path, void* stream);
+
+/* Insertion of new tokens into the NVFP4 caches, the step before the decode path
+ * [vLLM-zh "QKV GEMM + norm + RoPE + KV insert fusion": the projection epilogue
+ * takes the FP32 accumulators head by head, quantises K, V and the index keys to
+ * NVFP4 and writes them straight into their caches]. This is that epilogue's
+ * quantise-and-write half on its own.
+ *
+ * Token t goes to page slot_mapping[t] / 128, slot slot_mapping[t] % 128: its 4 K
+ * rows (k[t][h], h = KV head), 4 V rows and its index-key row are each quantised to
+ * NVFP4 and written to that slot of k_data/k_scale, v_data/v_scale and
+ * ki_data/ki_scale (layouts above). NVFP4 per 16 consecutive elements: scale =
+ * amax / 6 rounded to E4M3 (nearest, ties to even, saturating at 448); element code
+ * = the E2M1 value nearest x / scale (ties to the even code, saturating at 6) with
+ * the sign of x (so -0.0 and small negative values give code 8); a zero scale
+ * gives zero codes. The kernel decides every rounding by exact comparisons, so the
+ * bytes equal an exact evaluation of that rule for every finite input; inputs must
+ * be finite.
+ *
+ * A negative slot skips the token. A NULL source (k, v or k_idx) leaves its cache
+ * untouched (its cache pointers may then be NULL). Tokens whose page is outside
+ * [0, num_pages) are skipped and set MSA_FLAG_BAD_SLOT in the workspace
+ * (msa_get_error). Two tokens mapped to the same slot race; the caller keeps slots
+ * distinct. Sources must be 16-byte aligned; ws is any workspace of at least 256
+ * bytes, 256-byte aligned and zero-filled once (its first word holds the flags).
+ * All pointers are device pointers owned by the caller. */
+typedef struct {
+  int32_t num_tokens;           /* T >= 0 */
+  int32_t num_pages;            /* P, pages in each cache */
+  const int64_t* slot_mapping;  /* [T] page * 128 + slot, negative = skip */
+  const float* k;               /* [T][4][128] FP32, or NULL */
+  const float* v;               /* [T][4][128] FP32, or NULL */
+  const float* k_idx;           /* [T][128] FP32, or NULL */
+  uint8_t* k_data;
+  uint8_t* k_scale;
+  uint8_t* v_data;
+  uint8_t* v_scale;
+  uint8_t* ki_data;
+  uint8_t* ki_scale;
+} msa_kv_insert_args;
+
+msa_status msa_kv_insert_nvfp4(const msa_kv_insert_args* args, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

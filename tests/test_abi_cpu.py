@@ -21,7 +21,7 @@ def lib():
 def declared():
     text = open(os.path.join(ROOT, "include", "msa.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -72,3 +72,22 @@ def test_null_pointer_arguments(lib):
     assert lib.msa_workspace_init(None, 0, None) == -4
     a = _args()
     assert lib.msa_decode(ctypes.byref(a), None, None, None, None, 0, None) == -1
+
+
+def test_kv_insert_host_validation(lib):
+    """msa_kv_insert_nvfp4 rejects bad arguments before any CUDA call."""
+    A = _lib.KvInsertArgs
+    f = lib.msa_kv_insert_nvfp4
+    ws = ctypes.c_void_p(1 << 20)                       # never dereferenced: checks fail first
+    assert f(None, ws, 256, None) == -1
+    a = A(num_tokens=-1, num_pages=1)
+    assert f(ctypes.byref(a), ws, 256, None) == -1
+    a = A(num_tokens=4, num_pages=1)                    # no slot mapping
+    assert f(ctypes.byref(a), ws, 256, None) == -1
+    a = A(num_tokens=4, num_pages=1, slot_mapping=1 << 20, k=(1 << 20) + 4, k_data=1 << 21, k_scale=1 << 22)
+    assert f(ctypes.byref(a), ws, 256, None) == -1       # source not 16-byte aligned
+    a = A(num_tokens=4, num_pages=1, slot_mapping=1 << 20, k=1 << 20)
+    assert f(ctypes.byref(a), ws, 256, None) == -1       # source without its cache
+    a = A(num_tokens=4, num_pages=1, slot_mapping=1 << 20, k=1 << 20, k_data=1 << 21, k_scale=1 << 22)
+    assert f(ctypes.byref(a), None, 256, None) == -4     # no workspace
+    assert f(ctypes.byref(a), ws, 16, None) == -4        # workspace too small
