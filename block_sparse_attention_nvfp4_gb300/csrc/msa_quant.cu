@@ -11,20 +11,21 @@
 // x / scale (ties to the even code, saturating at 6) with the sign of x; a zero
 // scale gives zero codes.
 //
-// Both roundings are decided by exact FP32 comparisons, so the result equals an
-// exact (real-number) evaluation for every finite input:
+// Both roundings equal an exact (real-number) evaluation for every finite input:
 //  * scale: the hardware conversion of fl(amax * (1/6)) (relative error below
 //    2^-22) is at most one code away from the exact rounding; it is corrected by
 //    comparing amax with 6 x the midpoints to its neighbours. Two neighbouring E4M3
 //    values sum to at most 5 significant bits, times 3 at most 7: exact in FP32.
-//  * codes: |x| is compared with t x scale for the midpoints t of the E2M1 grid
-//    (0.25 .. 5, at most 3 significant bits; the scale at most 4): exact. A
-//    three-level search takes >= at the first two levels and > at the third, which
-//    sends each tie to the even code.
+//  * codes: x / scale correctly rounded to FP32 (reciprocal rounded to nearest, one
+//    FMA residual and one FMA correction: Markstein's division), then the hardware
+//    round-to-nearest-even conversion to E2M1. The double rounding is harmless: with
+//    at most 4 significant bits in the scale, the rounded quotient equals an E2M1
+//    midpoint (0.25, 0.75, .. 5) only when x / scale equals it exactly, and lies on
+//    the same side of every midpoint as the exact quotient.
 //
-// Layout: one warp per 128-element row (lane = 4 consecutive elements, 4 lanes = one
-// 16-element group), rows numbered token * 9 + {0..3: K heads, 4..7: V heads,
-// 8: index key}; a warp takes kRows rows per pass and issues their loads first.
+// Layout: one warp per token; lane = 4 consecutive elements of each of the token's 9
+// rows (4 K heads, 4 V heads, the index key), 4 lanes = one 16-element group. All 9
+// rows' loads are issued before the token's slot is examined.
 #include <cstdint>
 
 #include "msa_common.cuh"
@@ -34,9 +35,7 @@ namespace msa {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantCtasPerSm = 4;  // 32 warps x 4 rows x 512 B = 64 KB of loads in flight per SM
-constexpr int kRows = 4;           // rows per warp per pass
-constexpr int kRowsPerToken = 9;   // 4 K heads, 4 V heads, 1 index key
+constexpr int kQuantCtasPerSm = 3;  // 24 warps x 9 rows x 512 B = 110 KB of loads in flight per SM
 
 // E4M3 code 0..126 (non-negative, finite) to its FP32 value, from the bits.
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
@@ -59,79 +58,69 @@ __device__ __forceinline__ uint32_t scale_code(float amax) {
   return c;
 }
 
-// E2M1 magnitude code (0..7) of |x| / sv, given the midpoint products t x sv.
-struct E2m1Thresholds {
-  float t025, t075, t125, t175, t25, t35, t5;
-};
-__device__ __forceinline__ uint32_t e2m1_code(float x, const E2m1Thresholds& t) {
-  const float a = fabsf(x);
-  const bool b2 = a >= t.t175;                        // codes 4..7 (tie 1.75 -> 4)
-  const bool b1 = a >= (b2 ? t.t35 : t.t075);         // 6..7 | 2..3 (ties 3.5 -> 6, 0.75 -> 2)
-  const float t3 = b2 ? (b1 ? t.t5 : t.t25) : (b1 ? t.t125 : t.t025);
-  const bool b0 = a > t3;                             // ties 5 -> 6, 2.5 -> 4, 1.25 -> 2, 0.25 -> 0
-  return (b2 ? 4u : 0u) | (b1 ? 2u : 0u) | (b0 ? 1u : 0u) | ((__float_as_uint(x) >> 28) & 8u);
+// x / sv correctly rounded, given inv = 1 / sv rounded to nearest; the sign is put back
+// for x = -0.0, whose correction step would give +0.0 (-0 + +0 = +0).
+__device__ __forceinline__ float div_rn(float x, float sv, float inv) {
+  const float q = x * inv;
+  return copysignf(fmaf(fmaf(-q, sv, x), inv, q), x);
+}
+
+// Two E2M1 codes (sign in bit 3) of x0 / sv (low nibble) and x1 / sv (high nibble).
+__device__ __forceinline__ uint32_t e2m1x2(float x0, float x1, float sv, float inv) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+      : "=r"(r)
+      : "f"(div_rn(x1, sv, inv)), "f"(div_rn(x0, sv, inv)));
+  return r & 0xFFu;
+}
+
+// Quantise this lane's 4 elements of a 128-element row and store them (2 code bytes)
+// with the group's scale byte (lanes 4g store scale g).
+__device__ __forceinline__ void quantize_store(const float4& x, uint8_t* codes, uint8_t* scales, int lane) {
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+  const uint32_t sc = scale_code(amax);
+  const float sv = e4m3_value(sc);
+  const float inv = __frcp_rn(sv);
+  uint32_t c = e2m1x2(x.x, x.y, sv, inv) | (e2m1x2(x.z, x.w, sv, inv) << 8);
+  if (sv == 0.f) c = 0u;  // a zero scale gives zero codes
+  reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(c);
+  if ((lane & 3) == 0) scales[lane >> 2] = static_cast<uint8_t>(sc);
 }
 
 __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) kv_insert_kernel(const KvInsertParams p) {
   const int lane = threadIdx.x & 31;
-  const long long nrows = p.num_tokens * kRowsPerToken;
-  const long long warp0 = (static_cast<long long>(blockIdx.x) * kQuantThreads + threadIdx.x) >> 5;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * kQuantThreads) >> 5;
-  for (long long r0 = warp0 * kRows; r0 < nrows; r0 += nwarps * kRows) {
-    float4 x[kRows];
-    uint8_t* dst_code[kRows];
-    uint8_t* dst_scale[kRows];
+  const long long nwarps = static_cast<long long>(gridDim.x) * (kQuantThreads / 32);
+  for (long long t = static_cast<long long>(blockIdx.x) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+       t < p.num_tokens; t += nwarps) {
+    const long long sl = p.slot_mapping[t];
+    float4 xk[kGroups], xv[kGroups], xi;
+    if (p.k != nullptr)
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      dst_code[i] = nullptr;
-      dst_scale[i] = nullptr;
-      const long long r = r0 + i;
-      if (r >= nrows) continue;
-      const long long t = r / kRowsPerToken;
-      const int kind = static_cast<int>(r - t * kRowsPerToken);
-      const long long sl = p.slot_mapping[t];
-      if (sl < 0) continue;
-      const long long page = sl >> 7, slot = sl & 127;
-      if (page >= p.num_pages) {
-        if (lane == 0 && kind == 0) set_flag(p.flags, kFlagBadSlot);
-        continue;
-      }
-      const float* src;
-      if (kind < kGroups) {
-        if (p.k == nullptr) continue;
-        src = p.k + (t * kGroups + kind) * kDim;
-        const long long row = (page * kGroups + kind) * kBlock + slot;
-        dst_code[i] = p.k_data + row * 64;
-        dst_scale[i] = p.k_scale + row * 8;
-      } else if (kind < 2 * kGroups) {
-        if (p.v == nullptr) continue;
-        src = p.v + (t * kGroups + (kind - kGroups)) * kDim;
-        const long long row = (page * kGroups + (kind - kGroups)) * kBlock + slot;
-        dst_code[i] = p.v_data + row * 64;
-        dst_scale[i] = p.v_scale + row * 8;
-      } else {
-        if (p.ki == nullptr) continue;
-        src = p.ki + t * kDim;
-        const long long row = page * kBlock + slot;
-        dst_code[i] = p.ki_data + row * 64;
-        dst_scale[i] = p.ki_scale + row * 8;
-      }
-      x[i] = __ldcs(reinterpret_cast<const float4*>(src) + lane);  // read once: streaming
+      for (int h = 0; h < kGroups; ++h) xk[h] = __ldcs(reinterpret_cast<const float4*>(p.k + (t * kGroups + h) * kDim) + lane);
+    if (p.v != nullptr)
+#pragma unroll
+      for (int h = 0; h < kGroups; ++h) xv[h] = __ldcs(reinterpret_cast<const float4*>(p.v + (t * kGroups + h) * kDim) + lane);
+    if (p.ki != nullptr) xi = __ldcs(reinterpret_cast<const float4*>(p.ki + t * kDim) + lane);
+    if (sl < 0) continue;
+    const long long page = sl >> 7, slot = sl & 127;
+    if (page >= p.num_pages) {
+      if (lane == 0) set_flag(p.flags, kFlagBadSlot);
+      continue;
     }
+    const long long kv_row = page * kGroups * kBlock + slot;  // + h * kBlock for KV head h
+    if (p.k != nullptr)
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      if (dst_code[i] == nullptr) continue;  // warp-uniform
-      float amax = fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w)));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-      const uint32_t sc = scale_code(amax);
-      const float sv = e4m3_value(sc);
-      const E2m1Thresholds th = {0.25f * sv, 0.75f * sv, 1.25f * sv, 1.75f * sv, 2.5f * sv, 3.5f * sv, 5.f * sv};
-      uint32_t codes = e2m1_code(x[i].x, th) | (e2m1_code(x[i].y, th) << 4) | (e2m1_code(x[i].z, th) << 8) |
-                       (e2m1_code(x[i].w, th) << 12);
-      if (sv == 0.f) codes = 0u;
-      reinterpret_cast<uint16_t*>(dst_code[i])[lane] = static_cast<uint16_t>(codes);
-      if ((lane & 3) == 0) dst_scale[i][lane >> 2] = static_cast<uint8_t>(sc);
+      for (int h = 0; h < kGroups; ++h)
+        quantize_store(xk[h], p.k_data + (kv_row + h * kBlock) * 64, p.k_scale + (kv_row + h * kBlock) * 8, lane);
+    if (p.v != nullptr)
+#pragma unroll
+      for (int h = 0; h < kGroups; ++h)
+        quantize_store(xv[h], p.v_data + (kv_row + h * kBlock) * 64, p.v_scale + (kv_row + h * kBlock) * 8, lane);
+    if (p.ki != nullptr) {
+      const long long ki_row = page * kBlock + slot;
+      quantize_store(xi, p.ki_data + ki_row * 64, p.ki_scale + ki_row * 8, lane);
     }
   }
 }
@@ -139,9 +128,7 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) kv_insert_kern
 }  // namespace
 
 cudaError_t launch_kv_insert(const KvInsertParams& prm, int sm_count, cudaStream_t st) {
-  const long long rows = prm.num_tokens * kRowsPerToken;
-  const long long warps_needed = (rows + kRows - 1) / kRows;
-  const long long blocks_needed = (warps_needed + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+  const long long blocks_needed = (prm.num_tokens + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
   const long long cap = static_cast<long long>(sm_count) * kQuantCtasPerSm;  // one full wave
   const int grid = static_cast<int>(blocks_needed < cap ? blocks_needed : cap);
   if (grid <= 0) return cudaSuccess;

@@ -34,9 +34,9 @@ def _rows(rng, n):
 
 def _adversarial(rng, rows):
     """Overwrite groups of `rows` with the cases where rounding is decided by a hair:
-    amax / 6 exactly at and one FP32 ulp around an E4M3 midpoint; elements exactly at
-    and one ulp around t x scale for every E2M1 midpoint t; zero, tiny, huge and
-    negative-zero groups."""
+    amax / 6 exactly at and one FP32 ulp around every E4M3 midpoint; elements exactly at
+    and 1..3 ulps around t x scale for every E2M1 midpoint t and every scale; zero, tiny,
+    huge and negative-zero groups."""
     g = rows.reshape(-1, 16)
     n = g.shape[0]
     idx = rng.permutation(n)
@@ -49,17 +49,27 @@ def _adversarial(rng, rows):
             grp[rng.integers(16)] = a * (1 if rng.random() < 0.5 else -1)
             g[idx[k]] = grp
             k += 1
-    for _ in range(120):                                 # element ties at t x scale
-        s = E4M3[rng.integers(1, 127)]
-        grp = np.empty(16, np.float32)
-        grp[0] = np.float32(6.0 * s)                     # amax = 6 s exactly, so the scale is s
-        t = E2M1_MID[rng.integers(0, 7, size=15)] * s
-        d = rng.integers(-1, 2, size=15)
-        v = t.astype(np.float32)
-        v = np.where(d < 0, np.nextafter(v, np.float32(-np.inf)), np.where(d > 0, np.nextafter(v, np.float32(np.inf)), v))
-        grp[1:] = v * np.where(rng.random(15) < 0.5, -1, 1).astype(np.float32)
-        g[idx[k]] = grp
-        k += 1
+    # element ties: for every scale s, elements at t x s and 1..3 FP32 ulps either side,
+    # for every E2M1 midpoint t, in groups whose first element 6 s fixes the scale at s
+    offs = np.arange(-3, 4)
+    for sc in range(1, 127):
+        s = E4M3[sc]
+        vals = []
+        for t in E2M1_MID:
+            base = np.float32(t * s)
+            for o in offs:
+                v = base
+                for _ in range(abs(o)):
+                    v = np.nextafter(v, np.float32(np.inf if o > 0 else -np.inf))
+                vals.append(v if rng.random() < 0.5 else -v)
+        vals = np.array(vals, np.float32)
+        for j in range(0, len(vals), 15):
+            grp = np.zeros(16, np.float32)
+            grp[0] = np.float32(6.0 * s)                 # amax = 6 s exactly, so the scale is s
+            chunk = vals[j:j + 15]
+            grp[1:1 + len(chunk)] = chunk
+            g[idx[k]] = grp
+            k += 1
     g[idx[k]] = 0.0
     g[idx[k + 1]] = np.float32(1e-4) * rng.uniform(-1, 1, 16).astype(np.float32)   # scale rounds to 0
     g[idx[k + 2]] = rng.uniform(-1, 1, 16).astype(np.float32) * np.float32(1e30)   # saturating scale
