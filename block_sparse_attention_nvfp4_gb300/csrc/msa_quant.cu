@@ -35,7 +35,7 @@ namespace msa {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantCtasPerSm = 3;  // 24 warps x 9 rows x 512 B = 110 KB of loads in flight per SM
+constexpr int kQuantCtasPerSm = 4;  // 32 warps x 9 rows x 512 B = 110 KB of loads in flight per SM
 
 // E4M3 code 0..126 (non-negative, finite) to its FP32 value, from the bits.
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
@@ -50,9 +50,14 @@ __device__ __forceinline__ uint32_t scale_code(float amax) {
       : "=r"(pair)
       : "f"(0.f), "f"(amax * (1.f / 6.f)));
   uint32_t c = pair & 0xFFu;  // the second operand lands in the low byte
+  const uint32_t e = c >> 3, m = c & 7u;
   const float vc = e4m3_value(c);
-  const float up = c < 126u ? 3.f * (vc + e4m3_value(c + 1u)) : __int_as_float(0x7f800000);  // 6 x midpoint
-  const float dn = c > 0u ? 3.f * (e4m3_value(c - 1u) + vc) : -1.f;
+  // grid spacing at c: 2^(e-10), 2^-9 for the subnormals; the spacing below c is half
+  // of it when c is a power of two above the first binade (m = 0, e >= 2). 6 x the
+  // midpoints: 6 vc +- 3 x spacing, at most 7 significant bits: exact.
+  const float sp = __uint_as_float((e > 0u ? e + 117u : 118u) << 23);
+  const float up = c < 126u ? fmaf(6.f, vc, 3.f * sp) : __int_as_float(0x7f800000);
+  const float dn = c > 0u ? fmaf(6.f, vc, (m == 0u && e >= 2u) ? -1.5f * sp : -3.f * sp) : -1.f;
   if (amax > up || (amax == up && (c & 1u))) ++c;
   else if (amax < dn || (amax == dn && (c & 1u))) --c;
   return c;
