@@ -304,34 +304,26 @@ def run_libmsa(args, rank, world, dist):
                 "frac": round(achieved / peak, 4), "traffic": profile_traffic("select_kernel", args.workload),
                 "algorithmic_bytes_per_launch": sel_bytes, "avg_launch_us": round(sel_ms * 1e3, 2)}
 
-    # ---- end to end through the public API: host buffers, copies inside the timed region
+    # ---- end to end through the public API: a step from pinned host memory (HostIO: the
+    # inputs packed into one buffer, one host-to-device copy, the decode, one
+    # device-to-host copy of the packed outputs, synchronize), copies inside the timed region
     ke = min(args.steps, 50)
-    h_in = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
-            for k in ("context_lens", "q_indptr", "block_table", "q", "q_idx")}
-    h_out = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
-    h_ids = torch.empty(dec.block_ids.shape, dtype=dec.block_ids.dtype).pin_memory()
-    h_lse = torch.empty(dec.lse.shape, dtype=dec.lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_ids, h_lse))
+    io = dec.host_io()
     torch.cuda.synchronize()
     e2e_times = []
     for i in range(ke + 2):
         l2_flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for k, t in h_in.items():
-            getattr(batch, k).copy_(t, non_blocking=True)
-        dec.decode()
-        h_out.copy_(dec.out, non_blocking=True)
-        h_ids.copy_(dec.block_ids, non_blocking=True)
-        h_lse.copy_(dec.lse, non_blocking=True)
-        torch.cuda.synchronize()
+        io.step()
         if i >= 2:
             e2e_times.append(time.perf_counter() - t0)
+    assert torch.equal(io.outputs["block_ids"], ids_now.cpu()), "host-path ids differ from the device path's"
     e2e_t, e2e_u = reduce_over_ranks(sum(e2e_times), float(rows * ke), dist)
-    e2e = {"value": round(e2e_u / e2e_t, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "steps": ke,
-           "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4)}
+    e2e = {"value": round(e2e_u / e2e_t, 1), "unit": UNIT, "h2d_bytes_per_step": int(io.h2d_bytes),
+           "d2h_bytes_per_step": int(io.d2h_bytes), "steps": ke,
+           "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
+           "path": "MSADecoder.host_io().step(): 1 H2D copy, 3 kernels, 1 D2H copy, synchronize"}
 
     # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample
     cpu = None

@@ -180,6 +180,11 @@ def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tenso
                                          ws.numel() * ws.element_size(), _stream(stream)), "msa_sparse_attn_decode")
 
 
+def msa_decode_ptrs(args: Args, ids_p, out_p, lse_p, ws_p, ws_bytes: int, stream=None):
+    """msa_decode with already-marshalled device pointers (ctypes.c_void_p or None)."""
+    _check(load().msa_decode(ctypes.byref(args), ids_p, out_p, lse_p, ws_p, ws_bytes, _stream(stream)), "msa_decode")
+
+
 def msa_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],
                ws: torch.Tensor, stream=None):
     _check(load().msa_decode(ctypes.byref(args), _ptr(block_ids), _ptr(out), _ptr(lse), _ptr(ws),

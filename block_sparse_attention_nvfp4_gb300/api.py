@@ -93,8 +93,18 @@ class MSADecoder:
         self.args = _lib.make_args(self.cache, batch, self.sm_scale)
 
     def decode(self, stream=None):
-        _lib.msa_decode(self.args, self.block_ids, self.out.view(torch.int16), self.lse, self.ws, stream)
+        fast = getattr(self, "_decode_ptrs", None)
+        if fast is None or fast[0] is not self.args:
+            # the outputs and the workspace never move: marshal their pointers once
+            fast = (self.args, _lib._ptr(self.block_ids), _lib._ptr(self.out.view(torch.int16)), _lib._ptr(self.lse),
+                    _lib._ptr(self.ws), self.ws.numel() * self.ws.element_size())
+            self._decode_ptrs = fast
+        _lib.msa_decode_ptrs(*fast, stream)
         return self.out, self.block_ids
+
+    def host_io(self) -> "HostIO":
+        """Pinned host staging for whole decode steps from host memory (see HostIO)."""
+        return HostIO(self)
 
     def select_blocks(self, stream=None):
         _lib.msa_select_blocks(self.args, self.block_ids, self.block_scores, self.ws, stream)
@@ -123,3 +133,60 @@ def dequant_rows(codes: torch.Tensor, scales: torch.Tensor, path: int = 0) -> to
     out = torch.empty((codes.shape[0], 128), dtype=torch.uint8, device=codes.device)
     _lib.msa_dequant_rows(codes, scales, out, path)
     return out
+
+
+def _packed(specs, device, pin):
+    """One uint8 buffer holding the listed (name, shape, dtype) tensors at 256-byte aligned
+    offsets; returns (buffer, {name: view})."""
+    off, places = 0, []
+    for name, shape, dtype in specs:
+        n = int(math.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        places.append((name, shape, dtype, off, n))
+        off += (n + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device, pin_memory=pin)
+    views = {name: buf[o:o + n].view(dtype).view(shape) for name, shape, dtype, o, n in places}
+    return buf, views
+
+
+class HostIO:
+    """A decode step from host memory with one copy each way.
+
+    The decoder's batch inputs (context_lens, q_indptr, block_table, q, q_idx) are moved into
+    one device buffer and its outputs (out, block_ids, lse) into another; `inputs` and
+    `outputs` are views of pinned host mirrors with the same layout. Fill `inputs`, call
+    `step()`: one host-to-device copy, the three decode kernels, one device-to-host copy,
+    all on `stream`, then a synchronize; `outputs` then hold the step's results."""
+
+    IN = ("context_lens", "q_indptr", "block_table", "q", "q_idx")
+
+    def __init__(self, dec: "MSADecoder"):
+        b = dec.batch
+        dev = b.q.device
+        spec_in = [(n, tuple(getattr(b, n).shape), getattr(b, n).dtype) for n in self.IN]
+        self.dev_in, dviews = _packed(spec_in, dev, False)
+        self.host_in, self.inputs = _packed(spec_in, "cpu", True)
+        for n in self.IN:
+            dviews[n].copy_(getattr(b, n))
+            self.inputs[n].copy_(getattr(b, n).cpu())
+        dec.rebind(DecodeBatch(dviews["context_lens"], dviews["q_indptr"], dviews["block_table"], dviews["q"],
+                               dviews["q_idx"], b.total_rows, b.max_rows_per_req))
+        spec_out = [("out", tuple(dec.out.shape), dec.out.dtype), ("block_ids", tuple(dec.block_ids.shape), torch.int32)]
+        if dec.lse is not None:
+            spec_out.append(("lse", tuple(dec.lse.shape), torch.float32))
+        self.dev_out, oviews = _packed(spec_out, dev, False)
+        self.host_out, self.outputs = _packed(spec_out, "cpu", True)
+        dec.out, dec.block_ids = oviews["out"], oviews["block_ids"]
+        dec.lse = oviews.get("lse")
+        dec._decode_ptrs = None  # the outputs moved: marshal again
+        self.dec = dec
+        self.h2d_bytes = self.host_in.numel()
+        self.d2h_bytes = self.host_out.numel()
+
+    def step(self, stream=None):
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            self.dev_in.copy_(self.host_in, non_blocking=True)
+            self.dec.decode(s)
+            self.host_out.copy_(self.dev_out, non_blocking=True)
+        s.synchronize()
+        return self.outputs

@@ -186,3 +186,21 @@ def test_presets_full_size(name):
         reqs = list(range(0, 64, 4))
     _, waived = _gpu.check_decode(wl, reqs)
     assert waived <= 2
+
+
+def test_host_io_step_matches_device_decode(ragged):
+    """MSADecoder.host_io(): one packed copy each way around the same decode gives the
+    device path's results exactly (the merge order does not depend on which split CTA
+    finishes last)."""
+    dec = _gpu.decoder(ragged)
+    out, ids = dec.decode()
+    torch.cuda.synchronize()
+    out_ref, ids_ref, lse_ref = out.clone().cpu(), ids.clone().cpu(), dec.lse.clone().cpu()
+    io = dec.host_io()
+    assert io.h2d_bytes >= sum(getattr(io.inputs[n], "nbytes", 0) for n in io.IN)
+    res = io.step()
+    assert torch.equal(res["block_ids"], ids_ref)
+    assert torch.equal(res["out"], out_ref)
+    assert torch.equal(res["lse"], lse_ref)
+    res = io.step()            # a second step from the same host inputs: same results
+    assert torch.equal(res["out"], out_ref)
