@@ -206,6 +206,7 @@ def measure_kv_insert(l2_flush, stream, reps: int, tokens: int = 131072, pages: 
     out = {"tokens": tokens, "rows": 9 * tokens, "us": round(us, 2), "algorithmic_bytes": nbytes,
            "achieved_gbs": round(gbs, 1), "peak_gbs": peak, "peak_source": peak_kind, "frac": round(gbs / peak, 4),
            "tokens_per_s": round(tokens / (us * 1e-6), 1), "launches": reps, "device_error_flags": flags,
+           "traffic": profile_traffic("kv_insert_kernel", f"insert_{tokens}"),
            "data": "synthetic: seeded N(0,1) FP32 rows on the device, shuffled slots"}
     del k, v, ki, cache
     torch.cuda.empty_cache()
