@@ -35,7 +35,7 @@ namespace msa {
 namespace {
 
 constexpr int kQuantThreads = 256;
-constexpr int kQuantCtasPerSm = 4;  // 32 warps x 9 rows x 512 B = 110 KB of loads in flight per SM
+constexpr int kQuantCtasPerSm = 3;  // 24 warps x 9 rows x 512 B = 110 KB of loads in flight per SM (80 registers)
 
 // E4M3 code 0..126 (non-negative, finite) to its FP32 value, from the bits.
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
@@ -79,19 +79,53 @@ __device__ __forceinline__ uint32_t e2m1x2(float x0, float x1, float sv, float i
   return r & 0xFFu;
 }
 
-// Quantise this lane's 4 elements of a 128-element row and store them (2 code bytes)
-// with the group's scale byte (lanes 4g store scale g).
-__device__ __forceinline__ void quantize_store(const float4& x, uint8_t* codes, uint8_t* scales, int lane) {
-  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  const uint32_t sc = scale_code(amax);
-  const float sv = e4m3_value(sc);
-  const float inv = __frcp_rn(sv);
+// Largest magnitude of this lane's 16-element group (4 lanes, 4 elements each).
+__device__ __forceinline__ float group_amax(const float4& x) {
+  float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+  return fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+}
+
+// Codes of this lane's 4 elements given its group's scale value and reciprocal, and the
+// stores: 2 code bytes per lane, the scale byte by lane 4g.
+__device__ __forceinline__ void codes_store(const float4& x, uint32_t sc, float sv, float inv, uint8_t* codes,
+                                            uint8_t* scales, int lane) {
   uint32_t c = e2m1x2(x.x, x.y, sv, inv) | (e2m1x2(x.z, x.w, sv, inv) << 8);
   if (sv == 0.f) c = 0u;  // a zero scale gives zero codes
   reinterpret_cast<uint16_t*>(codes)[lane] = static_cast<uint16_t>(c);
   if ((lane & 3) == 0) scales[lane >> 2] = static_cast<uint8_t>(sc);
+}
+
+// Quantise one 128-element row (this lane's 4 elements) and store it.
+__device__ __forceinline__ void quantize_store(const float4& x, uint8_t* codes, uint8_t* scales, int lane) {
+  const uint32_t sc = scale_code(group_amax(x));
+  const float sv = e4m3_value(sc);
+  codes_store(x, sc, sv, __frcp_rn(sv), codes, scales, lane);
+}
+
+// Four rows at once: their 32 group scales are rounded once each, lane 8j + g taking
+// row j's group g, then handed back to the 4 lanes of each group (the rounding and the
+// reciprocal are most of a row's work when every lane repeats them).
+__device__ __forceinline__ void quantize_store4(const float4 (&x)[4], uint8_t* const (&codes)[4],
+                                                uint8_t* const (&scales)[4], int lane) {
+  float am[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) am[j] = group_amax(x[j]);
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float t = __shfl_sync(0xFFFFFFFFu, am[j], 4 * (lane & 7));
+    if ((lane >> 3) == j) a = t;
+  }
+  const uint32_t sc = scale_code(a);
+  const float sv = e4m3_value(sc);
+  const float inv = __frcp_rn(sv);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int src = 8 * j + (lane >> 2);
+    codes_store(x[j], __shfl_sync(0xFFFFFFFFu, sc, src), __shfl_sync(0xFFFFFFFFu, sv, src),
+                __shfl_sync(0xFFFFFFFFu, inv, src), codes[j], scales[j], lane);
+  }
 }
 
 __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) kv_insert_kernel(const KvInsertParams p) {
@@ -115,14 +149,21 @@ __global__ void __launch_bounds__(kQuantThreads, kQuantCtasPerSm) kv_insert_kern
       continue;
     }
     const long long kv_row = page * kGroups * kBlock + slot;  // + h * kBlock for KV head h
-    if (p.k != nullptr)
-#pragma unroll
-      for (int h = 0; h < kGroups; ++h)
-        quantize_store(xk[h], p.k_data + (kv_row + h * kBlock) * 64, p.k_scale + (kv_row + h * kBlock) * 8, lane);
-    if (p.v != nullptr)
-#pragma unroll
-      for (int h = 0; h < kGroups; ++h)
-        quantize_store(xv[h], p.v_data + (kv_row + h * kBlock) * 64, p.v_scale + (kv_row + h * kBlock) * 8, lane);
+    static_assert(kGroups == 4, "the 4 KV heads are quantised together");
+    if (p.k != nullptr) {
+      uint8_t* const c[4] = {p.k_data + kv_row * 64, p.k_data + (kv_row + kBlock) * 64,
+                             p.k_data + (kv_row + 2 * kBlock) * 64, p.k_data + (kv_row + 3 * kBlock) * 64};
+      uint8_t* const sc[4] = {p.k_scale + kv_row * 8, p.k_scale + (kv_row + kBlock) * 8,
+                              p.k_scale + (kv_row + 2 * kBlock) * 8, p.k_scale + (kv_row + 3 * kBlock) * 8};
+      quantize_store4(xk, c, sc, lane);
+    }
+    if (p.v != nullptr) {
+      uint8_t* const c[4] = {p.v_data + kv_row * 64, p.v_data + (kv_row + kBlock) * 64,
+                             p.v_data + (kv_row + 2 * kBlock) * 64, p.v_data + (kv_row + 3 * kBlock) * 64};
+      uint8_t* const sc[4] = {p.v_scale + kv_row * 8, p.v_scale + (kv_row + kBlock) * 8,
+                              p.v_scale + (kv_row + 2 * kBlock) * 8, p.v_scale + (kv_row + 3 * kBlock) * 8};
+      quantize_store4(xv, c, sc, lane);
+    }
     if (p.ki != nullptr) {
       const long long ki_row = page * kBlock + slot;
       quantize_store(xi, p.ki_data + ki_row * 64, p.ki_scale + ki_row * 8, lane);
