@@ -49,7 +49,8 @@ class _Args(ctypes.Structure):
                 ("q", ctypes.c_void_p), ("q_idx", ctypes.c_void_p),
                 ("k_data", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("v_data", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("ki_data", ctypes.c_void_p), ("ki_scale", ctypes.c_void_p)]
+                ("ki_data", ctypes.c_void_p), ("ki_scale", ctypes.c_void_p),
+                ("exact_index_scores", ctypes.c_int32)]
 
 
 def _load():
@@ -68,6 +69,8 @@ def _load():
             lib.oracle_e4m3_round.argtypes = [ctypes.c_double]
             lib.oracle_dequant_value.restype = ctypes.c_double
             lib.oracle_dequant_value.argtypes = [ctypes.c_int, ctypes.c_int]
+            lib.oracle_dequant_value_exact.restype = ctypes.c_double
+            lib.oracle_dequant_value_exact.argtypes = [ctypes.c_int, ctypes.c_int]
             lib.oracle_dequant_table.argtypes = [dp]
             lib.oracle_token_scores.argtypes = [ap, ctypes.c_int, dp]
             lib.oracle_block_maxpool.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp]
@@ -99,7 +102,7 @@ def _c(a, dtype):
 class _Bound:
     """Keeps the numpy arrays alive while the C struct points at them."""
 
-    def __init__(self, wl):
+    def __init__(self, wl, exact: bool = False):
         self.arrs = {
             "context_lens": _c(wl.context_lens, np.int32), "q_indptr": _c(wl.q_indptr, np.int32),
             "block_table": _c(wl.block_table, np.int32), "q": _c(wl.q, np.uint8), "q_idx": _c(wl.q_idx, np.uint8),
@@ -109,7 +112,7 @@ class _Bound:
         }
         self.args = _Args(num_reqs=int(wl.num_reqs), num_pages=int(wl.num_pages),
                           max_pages_per_req=int(wl.max_pages_per_req), top_k=int(getattr(wl, "top_k", 16)),
-                          sm_scale=float(wl.sm_scale),
+                          sm_scale=float(wl.sm_scale), exact_index_scores=1 if exact else 0,
                           **{k: v.ctypes.data for k, v in self.arrs.items()})
 
     def ref(self):
@@ -147,6 +150,11 @@ def dequant_value(code: int, scale: int) -> float:
     return _load().oracle_dequant_value(int(code), int(scale))
 
 
+def dequant_value_exact(code: int, scale: int) -> float:
+    """E2M1(code) x E4M3(scale), not re-rounded (the exact-score indexer's key values)."""
+    return _load().oracle_dequant_value_exact(int(code), int(scale))
+
+
 def dequant_table() -> np.ndarray:
     """[256 scales, 16 codes] FP64 values the FP8 MMA consumes."""
     out = np.empty(256 * 16, np.float64)
@@ -162,11 +170,12 @@ def _geom(wl, b):
     return N, R
 
 
-def token_scores(wl, b: int) -> np.ndarray:
-    """Index scores of request b: [R, 4, N] FP64, -inf where a key lies after the row."""
+def token_scores(wl, b: int, exact: bool = False) -> np.ndarray:
+    """Index scores of request b: [R, 4, N] FP64, -inf where a key lies after the row.
+    exact=True: index keys dequantised without the E4M3 re-rounding (exact-score indexer)."""
     N, R = _geom(wl, b)
     out = np.empty(R * G * N + 1, np.float64)
-    bd = _Bound(wl)
+    bd = _Bound(wl, exact)
     _check(_load().oracle_token_scores(bd.ref(), b, _dp(out)), "token_scores")
     return out[:R * G * N].reshape(R, G, N)
 
@@ -181,11 +190,11 @@ def block_maxpool(token_s: np.ndarray) -> np.ndarray:
     return out[:G * nb].reshape(G, nb)
 
 
-def block_scores(wl, b: int) -> np.ndarray:
+def block_scores(wl, b: int, exact: bool = False) -> np.ndarray:
     N, R = _geom(wl, b)
     nb = (N + BLOCK - 1) // BLOCK
     out = np.empty(G * nb + 1, np.float64)
-    bd = _Bound(wl)
+    bd = _Bound(wl, exact)
     _check(_load().oracle_block_scores(bd.ref(), b, _dp(out)), "block_scores")
     return out[:G * nb].reshape(G, nb)
 

@@ -96,6 +96,14 @@ double oracle_dequant_value(int code, int scale_byte) {
   return oracle_e4m3_value(oracle_e4m3_round(oracle_e2m1_value(code) * oracle_e4m3_value(scale_byte)));
 }
 
+/* The exact value of one NVFP4 element: its E2M1 value times its E4M3 group scale,
+ * with no re-rounding. [vLLM-zh] "Rubin MSA kernels": dequantising to FP16 keeps the
+ * product exact and the scores free of the E4M3 re-rounding an FP8 MMA needs; the
+ * exact-score indexer computes the index scores from these values. */
+double oracle_dequant_value_exact(int code, int scale_byte) {
+  return oracle_e2m1_value(code) * oracle_e4m3_value(scale_byte);
+}
+
 /* All 256 scales x 16 codes, out[scale*16 + code]. The oracle looks values up
  * here instead of re-running the search per element; the table is the same
  * definition, evaluated once. */
@@ -109,6 +117,15 @@ void oracle_dequant_table(double* out) {
     g_dq_ready = 1;
   }
   if (out) memcpy(out, g_dq, sizeof(g_dq));
+}
+
+/* Exact dequantisation of one 128-element NVFP4 row (no E4M3 re-rounding). */
+static void dequant_row_exact(const uint8_t* codes, const uint8_t* scales, double* out) {
+  int i;
+  for (i = 0; i < OR_D; i++) {
+    int code = (i & 1) ? (codes[i / 2] >> 4) : (codes[i / 2] & 15);
+    out[i] = oracle_dequant_value_exact(code, scales[i / 16]);
+  }
 }
 
 /* Dequantise one 128-element NVFP4 row (64 code bytes, 8 scale bytes). */
@@ -132,6 +149,7 @@ typedef struct {
   const int32_t* block_table;
   const uint8_t *q, *q_idx;
   const uint8_t *k_data, *k_scale, *v_data, *v_scale, *ki_data, *ki_scale;
+  int32_t exact_index_scores; /* 1: index keys dequantised exactly (no E4M3 re-rounding) */
 } oracle_args;
 
 static int req_geometry(const oracle_args* a, int b, int* N, int* R, int* row0) {
@@ -169,7 +187,8 @@ int oracle_token_scores(const oracle_args* a, int b, double* s) {
   for (t = 0; t < N; t++) {
     int page = page_of(a, b, t / OR_BLK), slot = t % OR_BLK;
     if (page < 0) { free(qd); return OR_EINVAL; }
-    dequant_row(a->ki_data + ((int64_t)page * OR_BLK + slot) * 64, a->ki_scale + ((int64_t)page * OR_BLK + slot) * 8, kv);
+    (a->exact_index_scores ? dequant_row_exact : dequant_row)(a->ki_data + ((int64_t)page * OR_BLK + slot) * 64,
+                                                             a->ki_scale + ((int64_t)page * OR_BLK + slot) * 8, kv);
     for (r = 0; r < R; r++) {
       int pos = N - R + r;
       for (g = 0; g < OR_G; g++) {

@@ -59,6 +59,15 @@ def dequant(codes, scales):
     return _TAB[s.astype(np.int64), c.astype(np.int64)]
 
 
+def dequant_exact(codes, scales):
+    """Like dequant, without the E4M3 re-rounding: E2M1 value x E4M3 scale, exact in FP64."""
+    codes = np.asarray(codes)
+    lo, hi = codes & 15, codes >> 4
+    c = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (128,))
+    s = np.repeat(np.asarray(scales), 16, axis=-1)
+    return e2m1_table()[c.astype(np.int64)] * e4m3_values()[s.astype(np.int64)]
+
+
 def geom(wl, b):
     N = int(wl.context_lens[b])
     r0 = int(wl.q_indptr[b])
@@ -66,15 +75,15 @@ def geom(wl, b):
     return N, R, r0
 
 
-def keys_of(wl, b, which):
+def keys_of(wl, b, which, exact=False):
     """Dequantised keys of request b in logical order: index keys [N,128] or
-    K/V [N,4,128]."""
+    K/V [N,4,128]; exact=True (index keys): without the E4M3 re-rounding."""
     N, _, _ = geom(wl, b)
     t = np.arange(N)
     phys = wl.block_table[b, t // 128]
     slot = t % 128
     if which == "ki":
-        return dequant(wl.ki_data[phys, slot], wl.ki_scale[phys, slot])
+        return (dequant_exact if exact else dequant)(wl.ki_data[phys, slot], wl.ki_scale[phys, slot])
     data, scale = (wl.k_data, wl.k_scale) if which == "k" else (wl.v_data, wl.v_scale)
     return dequant(data[phys, :, slot], scale[phys, :, slot])
 
