@@ -284,6 +284,16 @@ def run_libmsa(args, rank, world, dist):
     torch.cuda.synchronize()
     sel_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     ids_now = dec.block_ids.clone()
+    # the exact-score selection (msa_select_blocks_exact), same flushing
+    evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
+    for i in range(kr):
+        l2_flush()
+        evx[i][0].record(stream)
+        dec.select_blocks_exact()
+        evx[i][1].record(stream)
+    torch.cuda.synchronize()
+    selx_ms = statistics.mean(a.elapsed_time(b) for a, b in evx)
+    dec.block_ids.copy_(ids_now)
     eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
     for i in range(kr):
         l2_flush()
@@ -349,6 +359,11 @@ def run_libmsa(args, rank, world, dist):
             "gpu_launches": 3 * args.steps,  # per step: index scan, top-k, sparse attention
             "kernels_us": {"decode": round(ms_per_step * 1e3, 2), "select": round(sel_ms * 1e3, 2),
                            "sparse_attention": round(attn_ms * 1e3, 2)},
+            "select_exact": {"us": round(selx_ms * 1e3, 2),
+                             "achieved_gbs": round(sel_bytes / (selx_ms * 1e-3) / 1e9, 1),
+                             "frac": round(sel_bytes / (selx_ms * 1e-3) / 1e9 / peak, 4),
+                             "what": "msa_select_blocks_exact: the same selection with exact index scores "
+                                     "(FP16 tiles and MMAs), timed alone like the roofline call"},
             "kv_insert_nvfp4": kv_insert,
             "clocks": clocks, "timed_wall_s": round(wall, 4), "device_error_flags": ok_flags,
             "impl": "libmsa"}

@@ -25,7 +25,7 @@ FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS, FLAG_BAD_SLOT = 0x1,
 # symbols include/msa.h declares (checked by the CPU tests)
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
-           "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4")
+           "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact")
 
 
 class MSAError(RuntimeError):
@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH):
             lib.msa_index_scores.argtypes = [ap, vp, i64, vp, sz, vp]
             lib.msa_block_maxpool_topk.argtypes = [ap, vp, i64, vp, vp, vp, sz, vp]
             lib.msa_select_blocks.argtypes = [ap, vp, vp, vp, sz, vp]
+            lib.msa_select_blocks_exact.argtypes = [ap, vp, vp, vp, sz, vp]
             lib.msa_select_blocks_noalloc.argtypes = [ap, vp, vp, vp]
             lib.msa_sparse_attn_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
@@ -164,6 +165,12 @@ def msa_select_blocks(args: Args, block_ids: torch.Tensor, block_scores: Optiona
                       stream=None):
     _check(load().msa_select_blocks(ctypes.byref(args), _ptr(block_ids), _ptr(block_scores), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "msa_select_blocks")
+
+
+def msa_select_blocks_exact(args: Args, block_ids: torch.Tensor, block_scores: Optional[torch.Tensor],
+                            ws: torch.Tensor, stream=None):
+    _check(load().msa_select_blocks_exact(ctypes.byref(args), _ptr(block_ids), _ptr(block_scores), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream)), "msa_select_blocks_exact")
 
 
 def msa_select_blocks_noalloc(args: Args, block_ids: torch.Tensor, block_scores: Optional[torch.Tensor],

@@ -110,6 +110,11 @@ class MSADecoder:
         _lib.msa_select_blocks(self.args, self.block_ids, self.block_scores, self.ws, stream)
         return self.block_ids
 
+    def select_blocks_exact(self, stream=None):
+        """Selection with exact index scores (msa_select_blocks_exact)."""
+        _lib.msa_select_blocks_exact(self.args, self.block_ids, self.block_scores, self.ws, stream)
+        return self.block_ids
+
     def sparse_attn(self, block_ids: torch.Tensor, stream=None):
         _lib.msa_sparse_attn_decode(self.args, block_ids, self.out.view(torch.int16), self.lse, self.ws, stream)
         return self.out

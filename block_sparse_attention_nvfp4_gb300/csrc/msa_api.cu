@@ -278,6 +278,9 @@ static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids
   DeviceInfo d;
   msa_status s = check_device(&d);
   if (s != MSA_OK) return s;
+  // the scan's shared memory grows with the request count (its page prefix); the exact-score
+  // layout leaves room for about 560 requests within the 227 KB a CTA may opt into
+  if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
   const Plan plan = make_plan(args->num_reqs, d.sm_count);
   Ws w;
   if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
@@ -288,7 +291,7 @@ static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids
   p.token_scores = tok;
   p.score_stride = stride;
   if (launch_select(map, p, mode, d.sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
-  if (mode == 0 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (mode != 1 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }
 
@@ -307,6 +310,14 @@ msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, fl
   if (s != MSA_OK) return s;
   if (block_ids == nullptr) return MSA_ERR_INVALID_ARG;
   return run_select(args, 0, block_ids, block_scores, nullptr, 0, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_select_blocks_exact(const msa_decode_args* args, int32_t* block_ids, float* block_scores, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, false, true);
+  if (s != MSA_OK) return s;
+  if (block_ids == nullptr) return MSA_ERR_INVALID_ARG;
+  return run_select(args, 2, block_ids, block_scores, nullptr, 0, ws, ws_bytes, static_cast<cudaStream_t>(stream));
 }
 
 msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scores, int64_t score_stride,

@@ -241,6 +241,15 @@ __device__ __forceinline__ void mma_f8_ws(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Weight-stationary form with F16 operands (K = 16 per instruction), both in shared memory.
+__device__ __forceinline__ void mma_f16_ws(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Instruction descriptor, kind::f16: F16 x F16 -> F32, K-major A, B K- or MN-major.
 __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N, bool b_mn) {
   return (1u << 4) | (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |

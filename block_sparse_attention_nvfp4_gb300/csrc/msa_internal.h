@@ -93,7 +93,7 @@ Plan make_plan(int num_reqs, int sm_count);
 int score_stride(int max_pages);  // block-score row length: max_pages rounded up to 4
 WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan);
 
-size_t select_smem_bytes(int num_reqs);
+size_t select_smem_bytes(int num_reqs, int mode);  // mode 2: the exact-score layout
 size_t attn_smem_bytes();
 // grid: a fixed number of CTAs per SM over `sm_count` SMs
 cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,

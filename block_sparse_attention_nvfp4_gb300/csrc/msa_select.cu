@@ -91,16 +91,21 @@ constexpr int kLutCopies = 16;                  // one per thread of a 16-thread
 static_assert(kDBufs * kDCols <= kTmemCols, "TMEM buffers exceed the allocation");
 static_assert(kDqWarp0 % 4 == 2 && kPoolWarp0 % 4 == 2, "each group of four warps covers the four lane quadrants");
 
-struct Smem {
+// MODE 2 (exact scores) keeps the index queries and the page tiles in FP16: each 128-element
+// row is two 64-element K chunks of 128 bytes, chunk c of a tile at c x (rows x 128 bytes).
+template <bool kExact>
+struct SmemT {
+  static constexpr uint32_t kTileB = kExact ? 2 * kTileBytes : kTileBytes;  // one page tile
+  static constexpr uint32_t kQB = kExact ? 2 * 32 * 128 : 32 * 128;         // one query tile
   int32_t phys[kCtaPages];                  // offset 0, 4 KB: this CTA's block-table entries (when they fit)
-  uint8_t qtile[kIssuers][32 * 128];        // offset 4 KB: A operands, one per MMA warp: index queries (SW128)
+  uint8_t qtile[kIssuers][kQB];             // A operands, one per MMA warp: index queries (SW128)
+  uint8_t codes[kStages][kCodeBytes];       // 1024-aligned
+  uint8_t tile[kBBufs][kTileB];             // B operand (SW128), 1024-aligned
+  uint8_t scales[kStages][kScaleBytes];
   // scaled magnitudes per scale magnitude, 16 interleaved copies (entry e of copy c
   // at 8 (16 e + c) bytes): the 16 threads of an 8-byte wavefront read 16
-  // different banks whatever their scales
-  uint2 lut[128 * kLutCopies];              // 16 KB
-  uint8_t codes[kStages][kCodeBytes];       // offset 24 KB, 1024-aligned
-  uint8_t tile[kBBufs][kTileBytes];         // B operand (SW128), 1024-aligned
-  uint8_t scales[kStages][kScaleBytes];
+  // different banks whatever their scales (the FP16 form needs no table)
+  uint2 lut[kExact ? 2 : 128 * kLutCopies];
   float part[kDBufs][4][kGroups];           // per D buffer: the pool warps' quadrant maxima per index group
   int2 page_bc[kDBufs];                     // per D buffer: (request, block) of its page
   uint64_t full[kStages], empty[kStages];
@@ -108,9 +113,13 @@ struct Smem {
   uint32_t taddr;
   uint32_t fma_k[4];                        // 65536, 16: constants the compiler cannot fold
 };
-static_assert(offsetof(Smem, qtile) % 1024 == 0, "swizzled A tile");
-static_assert(offsetof(Smem, codes) % 1024 == 0 && offsetof(Smem, tile) % 1024 == 0, "swizzled tiles");
-static_assert(offsetof(Smem, scales) % 16 == 0, "bulk copies need 16-byte alignment");
+using Smem = SmemT<false>;
+static_assert(offsetof(SmemT<false>, qtile) % 1024 == 0 && offsetof(SmemT<true>, qtile) % 1024 == 0, "swizzled A tile");
+static_assert(offsetof(SmemT<false>, codes) % 1024 == 0 && offsetof(SmemT<false>, tile) % 1024 == 0 &&
+                  offsetof(SmemT<true>, codes) % 1024 == 0 && offsetof(SmemT<true>, tile) % 1024 == 0,
+              "swizzled tiles");
+static_assert(offsetof(SmemT<false>, scales) % 16 == 0 && offsetof(SmemT<true>, scales) % 16 == 0,
+              "bulk copies need 16-byte alignment");
 
 struct PageCursor {
   int b;       // request
@@ -219,25 +228,72 @@ __device__ __forceinline__ void write_qtile(uint8_t* qtile, const uint8_t* q_idx
   }
 }
 
+// FP16 form of write_qtile (exact-score mode): row n's 128 E4M3 values widened to FP16
+// (exact) as two 64-element K chunks, chunk c at c x 4 KB, 16-byte piece p of a chunk row at
+// p ^ (n & 7).
+__device__ __forceinline__ void write_qtile_f16(uint8_t* qtile, const uint8_t* q_idx, int row0, int R, int t0,
+                                                int nthreads) {
+  for (int u = t0; u < 32 * 16; u += nthreads) {
+    const int nrow = u >> 4, piece = u & 15, c = piece >> 3, pc = piece & 7;
+    uint4 h = make_uint4(0u, 0u, 0u, 0u);
+    if (nrow < R * kGroups) {
+      const uint2 v =
+          *reinterpret_cast<const uint2*>(q_idx + (static_cast<long long>(row0) * kGroups + nrow) * kDim + piece * 8);
+      asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h.x) : "r"(v.x & 0xFFFFu));
+      asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h.y) : "r"(v.x >> 16));
+      asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h.z) : "r"(v.y & 0xFFFFu));
+      asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h.w) : "r"(v.y >> 16));
+    }
+    *reinterpret_cast<uint4*>(qtile + c * (32 * 128) + nrow * 128 + ((pc ^ (nrow & 7)) << 4)) = h;
+  }
+}
+
+// Exact-score dequantisation of one 64-element K chunk of a row: 8 code words (word i =
+// elements 8i .. 8i + 7, 16-element group i / 2 scaled by byte i / 2 of scw) to FP16, E2M1
+// value times the E4M3 scale, both exact in FP16 (at most 6 significant bits, |x| <= 2688),
+// stored as the chunk row's 8 16-byte pieces, piece i at i ^ (r & 7).
+__device__ __forceinline__ void dequant_f16_chunk(const uint32_t* w, uint32_t scw, uint32_t chunk_row, int r7) {
+  uint32_t s01, s23;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(s01) : "r"(scw & 0xFFFFu));
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(s23) : "r"(scw >> 16));
+  const uint32_t sq[4] = {prmt(s01, 0u, 0x1010u), prmt(s01, 0u, 0x3232u), prmt(s23, 0u, 0x1010u),
+                          prmt(s23, 0u, 0x3232u)};  // each group's scale in both halves
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t h[4];
+    asm("{ .reg .b8 a, b, c, d; mov.b32 {a, b, c, d}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, a; cvt.rn.f16x2.e2m1x2 %1, b; cvt.rn.f16x2.e2m1x2 %2, c; cvt.rn.f16x2.e2m1x2 %3, d; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w[i]));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) asm("mul.rn.f16x2 %0, %0, %1;" : "+r"(h[k]) : "r"(sq[i >> 1]));
+    st_shared_v4(chunk_row + (static_cast<uint32_t>(i ^ r7) << 4), h[0], h[1], h[2], h[3]);
+  }
+}
+
 }  // namespace
 
 // MODE 0: fused select (block scores + top-k). MODE 1: write per-token scores
-// (msa_index_scores) and stop.
+// (msa_index_scores) and stop. MODE 2: MODE 0 with exact index scores (FP16 tiles and
+// MMAs: the keys' E2M1 x scale values are not re-rounded to E4M3).
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     select_kernel(const __grid_constant__ CUtensorMap ki_map, const SelectParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem_al = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // TMA/UMMA tiles need 1 KB
-  Smem& sm = *reinterpret_cast<Smem*>(smem_al);
+  constexpr bool kExact = MODE == 2;
+  constexpr bool kPool = MODE != 1;  // block max pool + top-k (MODE 0, 2) vs per-token scores (MODE 1)
+  using Sm = SmemT<kExact>;
+  Sm& sm = *reinterpret_cast<Sm*>(smem_al);
   // page prefix over requests [B + 2]: counts first, then scanned in place. Only
   // requests that passed the checks below own pages, so the geometry of a page's
   // request is read from the (validated) inputs where it is needed.
-  long long* prefix = reinterpret_cast<long long*>(smem_al + sizeof(Smem));
+  long long* prefix = reinterpret_cast<long long*>(smem_al + sizeof(Sm));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.num_reqs;
 
-  if (MODE == 0) pdl_launch_dependents();
+  if (kPool) pdl_launch_dependents();
 
   // ---- per-request geometry (validated) and the page prefix sum
   for (int b = tid; b < B; b += kThreads) {
@@ -286,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (n <= 0) return;
 
   // ---- setup: table, barriers, tensor memory
-  for (int u = tid; u < 128 * kLutCopies; u += kThreads) sm.lut[u] = lut_magnitudes(static_cast<uint32_t>(u / kLutCopies));
+  if (!kExact)
+    for (int u = tid; u < 128 * kLutCopies; u += kThreads) sm.lut[u] = lut_magnitudes(static_cast<uint32_t>(u / kLutCopies));
   if (tid == 0) {
     sm.fma_k[0] = 65536u;
     sm.fma_k[1] = 16u;
@@ -315,8 +372,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // the first request's index queries
   const int first_req = cursor_at(p0, prefix, B).b;
   for (int m = 0; m < kIssuers; ++m)
-    write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[first_req], p.q_indptr[first_req + 1] - p.q_indptr[first_req], tid,
-                kThreads);
+    if (kExact)
+      write_qtile_f16(sm.qtile[m], p.q_idx, p.q_indptr[first_req], p.q_indptr[first_req + 1] - p.q_indptr[first_req],
+                      tid, kThreads);
+    else
+      write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[first_req], p.q_indptr[first_req + 1] - p.q_indptr[first_req], tid,
+                  kThreads);
   fence_proxy_async_smem();
   if (warp == kIssueWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
@@ -372,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // K step kk of an operand starts 32 bytes further: +2 in the start-address field
     const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sm.qtile[m]));
     const uint32_t tile0 = smem_u32(sm.tile[0]);
-    const uint32_t idesc = idesc_e4m3_f32(32, kBlock, false);
+    const uint32_t idesc = kExact ? idesc_f16_f32(32, kBlock, false) : idesc_e4m3_f32(32, kBlock, false);
     for (int i = m; i < n; i += kIssuers) {
       const int j = i % kBBufs, k = i % kDBufs;
       if (mm.b != qtile_req) {
@@ -384,7 +445,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           break;
         }
         tc_fence_after();
-        write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[mm.b], p.q_indptr[mm.b + 1] - p.q_indptr[mm.b], lane, 32);
+        if (kExact)
+          write_qtile_f16(sm.qtile[m], p.q_idx, p.q_indptr[mm.b], p.q_indptr[mm.b + 1] - p.q_indptr[mm.b], lane, 32);
+        else
+          write_qtile(sm.qtile[m], p.q_idx, p.q_indptr[mm.b], p.q_indptr[mm.b + 1] - p.q_indptr[mm.b], lane, 32);
         fence_proxy_async_smem();
         __syncwarp();
         qtile_req = mm.b;
@@ -394,10 +458,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (alive && i >= kDBufs) alive = wait_bar(smem_u32(&sm.dempty[k]), ((i / kDBufs) - 1) & 1, p.flags);
         if (alive) {
           tc_fence_after();
-          const uint64_t bdesc = sdesc_kmajor_sw128(tile0 + j * kTileBytes);
+          const uint64_t bdesc = sdesc_kmajor_sw128(tile0 + j * Sm::kTileB);
           const uint32_t d = tbase + k * kDCols;
+          if (kExact) {
+            // K step kk (16 FP16 elements, 32 bytes): chunk kk / 4 (4 KB of A, 16 KB of B
+            // further), +32 bytes per step inside it (start-address field in 16-byte units)
 #pragma unroll
-          for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ws(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
+            for (int kk = 0; kk < kDim / 16; ++kk)
+              mma_f16_ws(d, adesc + 256 * (kk >> 2) + 2 * (kk & 3), bdesc + 1024 * (kk >> 2) + 2 * (kk & 3), idesc,
+                         kk > 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kDim / 32; ++kk) mma_f8_ws(d, adesc + 2 * kk, bdesc + 2 * kk, idesc, kk > 0);
+          }
           mma_commit(smem_u32(&sm.dfull[k]));
           mma_commit(smem_u32(&sm.bfree[j]));
         }
@@ -442,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t d = d_lane + static_cast<uint32_t>(k) * kDCols;
       float m = -INFINITY;
       if (alive) {
-        if (MODE == 0 && N - R - t0 >= 31) {
+        if (kPool && N - R - t0 >= 31) {
           // every row sees the quadrant's 32 tokens (a warp-uniform test): the load's own
           // max reduction gives each row's maximum
           const float mq = tmem_ld32_max(d);
@@ -452,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           uint32_t v[32];
           tmem_ld32(d, v);
           tc_wait_ld();
-          if (MODE == 0) {
+          if (kPool) {
             if (rq < R) m = max32_masked(v, 0, lim);
           } else if (rq < R) {
             const int phys = staged ? sm.phys[ip] : p.block_table[static_cast<long long>(b) * p.max_pages + c];
@@ -467,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.dempty[k]));
-      if (MODE == 0) {
+      if (kPool) {
         // the group's maximum over its rows: lanes with equal lane % 4
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
@@ -526,9 +599,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (!alive) break;
         tc_fence_after();
       }
-      const uint32_t row_addr = tile0 + j * kTileBytes + row_off;
-      dequant_half_to_tile(lut_t, w, sc.x, k16, k4, row_addr, r7, 0);
-      dequant_half_to_tile(lut_t, w + 8, sc.y, k16, k4, row_addr, r7, 4);
+      const uint32_t row_addr = tile0 + j * Sm::kTileB + row_off;
+      if (kExact) {
+        dequant_f16_chunk(w, sc.x, row_addr, r7);                   // elements 0..63: K chunk 0
+        dequant_f16_chunk(w + 8, sc.y, row_addr + kTileBytes, r7);  // 64..127: chunk 1, 16 KB on
+      } else {
+        dequant_half_to_tile(lut_t, w, sc.x, k16, k4, row_addr, r7, 0);
+        dequant_half_to_tile(lut_t, w + 8, sc.y, k16, k4, row_addr, r7, 4);
+      }
       fence_proxy_async_smem();  // generic-proxy writes -> visible to the MMA (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.bfull[j]));
@@ -873,21 +951,25 @@ __global__ void dequant_rows_kernel(const uint8_t* codes, const uint8_t* scales,
   }
 }
 
-size_t select_smem_bytes(int num_reqs) {
-  const size_t need = sizeof(Smem) + sizeof(long long) * (num_reqs + 2) + 1024;
+size_t select_smem_bytes(int num_reqs, int mode) {
+  const size_t need = (mode == 2 ? sizeof(SmemT<true>) : sizeof(SmemT<false>)) + sizeof(long long) * (num_reqs + 2) + 1024;
   // more than half an SM's shared memory, so one CTA holds the SM's 512 tensor-memory columns
   return need > 120 * 1024 ? need : 120 * 1024;
 }
 
 cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, int mode, int sm_count,
                           cudaStream_t st) {
-  const size_t smem = select_smem_bytes(prm.num_reqs);
+  const size_t smem = select_smem_bytes(prm.num_reqs, mode);
   const int grid = kCtasPerSm * sm_count;
   cudaError_t e;
   if (mode == 0) {
     e = cudaFuncSetAttribute(select_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     select_kernel<0><<<grid, kThreads, smem, st>>>(ki_map, prm);
+  } else if (mode == 2) {
+    e = cudaFuncSetAttribute(select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    select_kernel<2><<<grid, kThreads, smem, st>>>(ki_map, prm);
   } else {
     e = cudaFuncSetAttribute(select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -154,6 +154,15 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
 msa_status msa_select_blocks(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* msa_select_blocks with exact index scores (the exact-score indexer) [vLLM-zh, Rubin MSA
+ * kernels: dequantising NVFP4 to FP16 keeps E2M1 x scale exact, so the scores are free of
+ * the E4M3 re-rounding an FP8 MMA implies]. The index keys' values are E2M1 x E4M3 scale
+ * exactly (FP16 operands, FP32 accumulation), the index queries their E4M3 values; pooling,
+ * top-k and the outputs are those of msa_select_blocks. Shared memory per CTA grows with
+ * num_reqs: more than about 560 requests return MSA_ERR_UNSUPPORTED. Same workspace. */
+msa_status msa_select_blocks_exact(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
+                                   void* ws, size_t ws_bytes, void* stream);
+
 /* Step 4 given block ids [B][4][16] (ascending or not, -1 = unused)
  * [vLLM-zh §How; MSA-fig §1 step 2]. out_bf16[row][32][128] (BF16 bits) gets
  * softmax attention over the keys of the listed blocks visible to the row; lse
