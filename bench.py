@@ -362,6 +362,7 @@ def run_libmsa(args, rank, world, dist):
             "select_exact": {"us": round(selx_ms * 1e3, 2),
                              "achieved_gbs": round(sel_bytes / (selx_ms * 1e-3) / 1e9, 1),
                              "frac": round(sel_bytes / (selx_ms * 1e-3) / 1e9 / peak, 4),
+                             "traffic_scan": profile_traffic("select_kernel_exact", args.workload),
                              "what": "msa_select_blocks_exact: the same selection with exact index scores "
                                      "(FP16 tiles and MMAs), timed alone like the roofline call"},
             "kv_insert_nvfp4": kv_insert,
