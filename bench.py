@@ -334,7 +334,9 @@ def run_libmsa(args, rank, world, dist):
     e2e = {"value": round(e2e_u / e2e_t, 1), "unit": UNIT, "h2d_bytes_per_step": int(io.h2d_bytes),
            "d2h_bytes_per_step": int(io.d2h_bytes), "steps": ke,
            "ms_per_step": round(1e3 * statistics.mean(e2e_times), 4),
-           "path": "MSADecoder.host_io().step(): 1 H2D copy, 3 kernels, 1 D2H copy, synchronize"}
+           "path": "MSADecoder.host_io().step(): 1 H2D copy, 3 kernels, 1 D2H copy, synchronize"
+                   + (", replayed as one CUDA graph" if io.graph is not None else
+                      f" (eager: graph capture failed: {io.graph_error})")}
 
     # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample
     cpu = None

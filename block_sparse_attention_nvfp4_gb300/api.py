@@ -187,11 +187,43 @@ class HostIO:
         self.h2d_bytes = self.host_in.numel()
         self.d2h_bytes = self.host_out.numel()
 
-    def step(self, stream=None):
+    def step(self, stream=None, graph: bool = True):
+        """One step: host inputs -> device, decode, outputs -> host, then synchronize. With
+        graph=True the step is captured once as a CUDA graph (the two copies and the three
+        kernels, their programmatic-launch chaining kept as graph edges) and replayed: one
+        launch per step instead of five. If capture is not possible the step runs eagerly
+        (`graph_error` says why)."""
         s = stream if stream is not None else torch.cuda.current_stream()
-        with torch.cuda.stream(s):
-            self.dev_in.copy_(self.host_in, non_blocking=True)
-            self.dec.decode(s)
-            self.host_out.copy_(self.dev_out, non_blocking=True)
+        if graph and self.graph is None and self.graph_error is None:
+            self._capture()
+        if graph and self.graph is not None:
+            with torch.cuda.stream(s):
+                self.graph.replay()
+        else:
+            with torch.cuda.stream(s):
+                self._enqueue(s)
         s.synchronize()
         return self.outputs
+
+    graph = None
+    graph_error = None
+
+    def _enqueue(self, s):
+        self.dev_in.copy_(self.host_in, non_blocking=True)
+        self.dec.decode(s)
+        self.host_out.copy_(self.dev_out, non_blocking=True)
+
+    def _capture(self):
+        torch.cuda.synchronize()
+        with torch.cuda.stream(torch.cuda.Stream()):
+            self._enqueue(torch.cuda.current_stream())  # attributes set, pointers marshalled
+        torch.cuda.synchronize()
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._enqueue(torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            self.graph = g
+        except Exception as e:  # keep the eager path
+            self.graph_error = repr(e)
+            torch.cuda.synchronize()

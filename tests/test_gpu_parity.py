@@ -204,3 +204,9 @@ def test_host_io_step_matches_device_decode(ragged):
     assert torch.equal(res["lse"], lse_ref)
     res = io.step()            # a second step from the same host inputs: same results
     assert torch.equal(res["out"], out_ref)
+    assert io.graph is not None, io.graph_error   # the steps above ran as a captured graph
+    res = io.step(graph=False)                    # and the eager path agrees
+    assert torch.equal(res["out"], out_ref) and torch.equal(res["block_ids"], ids_ref)
+    io.outputs["out"].zero_()
+    res = io.step()
+    assert torch.equal(res["out"], out_ref) and torch.equal(res["lse"], lse_ref)
