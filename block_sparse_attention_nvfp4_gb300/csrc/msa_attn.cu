@@ -207,22 +207,33 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_kernel(const AttnParams 
     *reinterpret_cast<uint4*>(sm.qtile + m * 128 + ((ch ^ (m & 7)) << 4)) = v;
   }
 
+  // the request's block-table row (an input) staged before the wait in the third K tile,
+  // unused until block 2 is dequantised, so the selected pages resolve from shared memory;
+  // the tensor memory too is taken before the wait (the SM's previous CTA, whose shared
+  // memory this CTA needed, has exited)
+  const bool bt_staged = nb <= static_cast<int>(kTileBytes / 4);
+  int32_t* bt = reinterpret_cast<int32_t*>(sm.ktile[2]);
+  if (bt_staged)
+    for (int c = tid; c < nb; c += kAttnThreads) bt[c] = p.block_table[static_cast<long long>(b) * p.max_pages + c];
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
+  __syncthreads();
+
   pdl_wait_primary();  // the block ids come from the selection
 
-  if (tid == 0) {
-    int n = 0;
-    for (int i = 0; i < kTopK; ++i) {
-      const int id = p.block_ids[(static_cast<long long>(b) * kGroups + g) * kTopK + i];
-      if (id >= 0 && id < nb) sm.ids[n++] = id;
-      else if (id != -1 && blockIdx.x == 0) set_flag(p.flags, kFlagBadIds);
+  if (warp == 0) {
+    // the 16 ids in parallel; the valid ones keep their order (ballot ranks)
+    const int id = lane < kTopK ? p.block_ids[(static_cast<long long>(b) * kGroups + g) * kTopK + lane] : -1;
+    const bool valid = lane < kTopK && id >= 0 && id < nb;
+    if (lane < kTopK && !valid && id != -1 && blockIdx.x == 0) set_flag(p.flags, kFlagBadIds);
+    const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
+    if (valid) {
+      const int rank = __popc(vm & ((1u << lane) - 1u));
+      sm.ids[rank] = id;
+      sm.phys[rank] = bt_staged ? bt[id] : p.block_table[static_cast<long long>(b) * p.max_pages + id];
     }
-    sm.nsel = n;
+    if (lane == 0) sm.nsel = __popc(vm);
   }
-  __syncthreads();
-  // the selected blocks' page ids, read once (not on the copy-issue path)
-  if (tid < sm.nsel) sm.phys[tid] = p.block_table[static_cast<long long>(b) * p.max_pages + sm.ids[tid]];
   fence_proxy_async_smem();
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(&sm.taddr), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
