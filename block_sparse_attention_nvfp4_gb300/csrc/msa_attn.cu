@@ -11,34 +11,38 @@
 // Design (GB300, tcgen05). Grid = (splits, request x group), one CTA per SM; a
 // CTA takes `blocks_per_split` of the group's selected blocks (flash-decoding
 // split over the selection). The group's 8R query rows (R speculative rows x 8
-// heads, at most 64) are the rows of a 128-row MMA tile:
+// heads, at most 64) are rows 0..63 of a 128-row MMA tile and again rows 64..127:
 //   * load warp: one lane copies each block's raw NVFP4 K and V (codes and
 //     scales) into a 2-stage shared-memory ring with bulk async copies;
-//   * 8 dequant warps, thread = one K row or one V row of the block: dequantise
-//     its 128 elements to E4M3 (byte-permute lookups in a table of scaled
-//     magnitudes) into a 128-byte-swizzled tile (V rows widened to FP16 into two
-//     64-dim tiles); three tile buffers;
+//   * 8 dequant warps, thread = one K row or one V row of the block (the two
+//     halves of the warps swap K and V every block, a V row costing about twice a
+//     K row): take the row's codes into registers and release the raw stage at
+//     once, then dequantise its 128 elements to E4M3 (byte-permute lookups in a
+//     table of scaled magnitudes) into a 128-byte-swizzled tile (V rows widened to
+//     FP16 into two 64-dim tiles); three tile buffers, K and V ready separately;
 //   * MMA warp: one lane issues S = Q K^T (FP8; A = query tile, B = K tile, both
 //     shared memory, K-major) into one of two TMEM score buffers, and O += P V
 //     (FP16; A = P from TMEM, B = the V tile read MN-major, so V is used in its
 //     stored key-major order without a transpose, as two 64-dim halves) into the
-//     TMEM output;
-//   * 4 softmax warps, two per query row (TMEM lane), each with half of the row's
-//     keys and half of its output dims: read the 64 scores once into registers,
-//     mask, exchange the half maxima through shared memory, online softmax (FP32
-//     running sum; exp2 in packed FP16, two keys per instruction, which is also
-//     the FP16 form P takes as the next MMA's A operand in TMEM). The exponent's
-//     reference point moves only when a block's max exceeds it by more than 2^8
-//     (so P <= 256 stays well inside FP16), and only then is the row's half of O
-//     in TMEM rescaled, after the previous P V has finished; O / l is exact
-//     whatever the reference. S = Q K^T of block j+1 runs while block j's
-//     softmax does.
+//     TMEM output; S of block j+2 is issued after P V of block j;
+//   * 4 softmax warps, one per SM sub-partition: warp q owns TMEM lanes 32q ..
+//     32q + 31 (query row 32 (q & 1) + lane) and keys 64 (q >> 1) .. + 63 of every
+//     block, so each warp holds whole rows for half the keys: read its 64 scores
+//     once into registers, mask, online softmax (FP32 running sum; exp2 in packed
+//     FP16, two keys per instruction, which is also the FP16 form P takes as the
+//     next MMA's A operand in TMEM; the P columns of the other key half stay zero
+//     in its lanes). The exponent's reference point moves only when a block's max
+//     exceeds it by more than 2^8 (so P <= 256 stays well inside FP16), and only
+//     then are the warp's O rows in TMEM rescaled, after the previous P V has
+//     finished; O / l is exact whatever the reference. The two key halves of a row
+//     are combined once, at the end, with the log-sum-exp rule.
 // P V runs in FP16: the dequantised V values (E4M3) are exact in FP16, and an
 // E4M3 P (3 mantissa bits) measurably misses 2e-2 relative accuracy on rows whose
 // weight sits on a few keys; FP16 P keeps 11 bits.
 // CTAs that split the selection write (o, lse) partials and the last one to
 // arrive for the (request, group) merges them with the exact log-sum-exp rule and
-// writes BF16 output.
+// writes BF16 output; finished rows go out through shared memory as coalesced
+// 16-byte stores.
 #include <cuda_bf16.h>
 
 #include <cstddef>

@@ -14,8 +14,8 @@
 // Both roundings equal an exact (real-number) evaluation for every finite input:
 //  * scale: the hardware conversion of fl(amax * (1/6)) (relative error below
 //    2^-22) is at most one code away from the exact rounding; it is corrected by
-//    comparing amax with 6 x the midpoints to its neighbours. Two neighbouring E4M3
-//    values sum to at most 5 significant bits, times 3 at most 7: exact in FP32.
+//    comparing amax with 6 x the midpoints to its neighbours, 6 v +- 3 x the grid
+//    spacing (at most 7 significant bits: exact in FP32).
 //  * codes: x / scale correctly rounded to FP32 (reciprocal rounded to nearest, one
 //    FMA residual and one FMA correction: Markstein's division), then the hardware
 //    round-to-nearest-even conversion to E2M1. The double rounding is harmless: with
@@ -25,7 +25,9 @@
 //
 // Layout: one warp per token; lane = 4 consecutive elements of each of the token's 9
 // rows (4 K heads, 4 V heads, the index key), 4 lanes = one 16-element group. All 9
-// rows' loads are issued before the token's slot is examined.
+// rows' loads are issued before the token's slot is examined. The 32 group scales of
+// the 4 K rows (and of the 4 V rows) are rounded once each, lane 8j + g taking row j's
+// group g, and handed back to the group's lanes by shuffles.
 #include <cstdint>
 
 #include "msa_common.cuh"

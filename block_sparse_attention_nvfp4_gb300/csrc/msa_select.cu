@@ -10,32 +10,29 @@
 // FP8 MMA [vLLM-zh, Blackwell kernels].
 //
 // Design (GB300, sm_103a). Decode reads the whole index-key cache every step, so
-// this kernel is a stream over the cache's pages at HBM speed. 2 CTAs per SM
-// (256 TMEM columns each), the grid taking equal contiguous ranges of all
-// requests' pages; one CTA has four roles:
-//   * load warp: one lane streams pages into a ring of shared-memory stages with
-//     TMA (codes: 2-D tensor copy with 64-byte swizzle, so each thread reads its
-//     64-byte row without bank conflicts; scales: 1-D bulk copy);
-//   * 8 dequant warps in two groups that take alternate pages (thread = token):
-//     dequantise the token's 128 elements to E4M3 (byte-permute table lookups for
-//     magnitudes and signs) and write them as row `token` of a page tile in
-//     shared memory (the MMA's B operand, K-major, 128-byte swizzle);
-//   * MMA warp: one lane issues, per page, D = Q x P^T with Q the request's
-//     4 x R index-query rows (A operand, M = 128 of which rows >= 32 are never
-//     read back) and P the dequantised page (N = 128 tokens, K = 128), FP32
-//     accumulation in tensor memory (products of two E4M3 values are exact; only
-//     the FP32 sums round); the warp rewrites Q when the request changes;
-//   * 2 epilogue warps taking alternate pages (D buffer e, TMEM lanes
-//     32e..32e+31 = the 32 query columns rq*4+g): read the page's 32 x 128
-//     scores, mask, take each row's maximum over the tokens and the group's
-//     maximum over its rows with shuffles, and write the block score.
-// Laying the scores out with the query columns on TMEM lanes puts a whole page's
-// max pool in one warp (no cross-warp combine); measured on GB300, the pool was
-// the costliest step when the 128 tokens were spread over four warps' lanes.
-// The dequant warps never wait for an MMA result, only for a free page tile, so
-// the MMA round trip hides behind the next pages' dequantisation.
-//
-// The top-k runs in a second kernel (one CTA per request, one warp per group),
+// this kernel is a stream over the cache's pages. One CTA per SM (896 threads, all
+// 512 TMEM columns), the grid taking equal contiguous ranges of all requests' pages;
+// the CTA's warps have four roles (details at the role constants below):
+//   * 2 load warps (one lane each, alternate pages): stream pages into a ring of
+//     shared-memory stages with TMA (codes: 2-D tensor copy with 64-byte swizzle, so
+//     each thread reads its 64-byte row without bank conflicts; scales: 1-D bulk);
+//   * 16 dequant warps in 4 groups taking pages round-robin (thread = token): take
+//     the token's codes into registers, release the stage, dequantise its 128
+//     elements to E4M3 (byte-permute table lookups for magnitudes and signs) and
+//     write them as row `token` of a page tile (the MMA's B operand, K-major,
+//     128-byte swizzle); MODE 2 writes the exact FP16 values instead;
+//   * 2 MMA warps (alternate pages, each with its own copy of the query tile): one
+//     lane issues, per page, the weight-stationary D = Q x P^T with Q the request's
+//     4 x R index-query rows (M = 32) and P the page (N = 128 tokens, K = 128), FP32
+//     accumulation in tensor memory (products of two E4M3 values, or of the FP16
+//     forms in MODE 2, are exact; only the FP32 sums round); the warp rewrites its
+//     query tile when the request changes;
+//   * 8 pool warps in 2 sets taking alternate pages, one warp per TMEM lane
+//     quadrant (= 32 of the page's tokens): the TMEM load's max reduction gives each
+//     query row's maximum over the quadrant's tokens (masked loads where the causal
+//     limit cuts the quadrant), shuffles give the group's maximum over its rows, and
+//     every 4 pages a set combines its quadrants into block scores.
+// The top-k runs in a second kernel (one CTA per request, four warps per group),
 // launched with programmatic dependent launch so its CTAs are resident and have
 // read the request geometry when the scan's last pages finish; it waits on the
 // scan's completion (griddepcontrol.wait), not on any flag another CTA writes.
