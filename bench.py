@@ -145,6 +145,32 @@ class ClockSampler:
                 "reasons": names, "samples": len(self.samples)}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def spread(ms):
+    """Median and spread of per-step times (ms) in microseconds."""
+    a = np.sort(np.asarray(ms, dtype=np.float64)) * 1e3
+    pick = lambda q: float(a[min(len(a) - 1, int(round(q * (len(a) - 1))))])  # noqa: E731
+    return {"median_us": round(pick(0.5), 2), "p10_us": round(pick(0.1), 2), "p90_us": round(pick(0.9), 2),
+            "min_us": round(float(a[0]), 2), "max_us": round(float(a[-1]), 2), "mean_us": round(float(a.mean()), 2)}
+
+
 def reduce_over_ranks(local_seconds: float, local_units: float, dist=None):
     """Whole-job numbers: units summed over ranks, time = the slowest rank's."""
     if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
@@ -213,6 +239,54 @@ def measure_kv_insert(l2_flush, stream, reps: int, tokens: int = 131072, pages: 
     return out
 
 
+def time_calls(fn, l2_flush, stream, reps):
+    """Per-call device times (ms) of fn() with the L2 flushed before each call (outside
+    the events)."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        l2_flush()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_preset(name, l2_flush, stream, reps, peak):
+    """One workload shape's decode step, selection call and attention alone (device
+    times, L2 flushed before each call, inputs resident), with its algorithmic bytes and
+    the step's fraction of the measured copy rate."""
+    import torch
+
+    from block_sparse_attention_nvfp4_gb300 import DecodeBatch, KVCache, MSADecoder
+    from block_sparse_attention_nvfp4_gb300 import bytes_model as bm
+    from block_sparse_attention_nvfp4_gb300 import synth
+
+    wl = synth.make_workload(synth.preset(name))
+    dec = MSADecoder(KVCache.from_host(wl), DecodeBatch.from_host(wl), sm_scale=wl.sm_scale, with_lse=True)
+    for _ in range(3):
+        l2_flush()
+        dec.decode()
+    torch.cuda.synchronize()
+    flags = dec.errors()
+    ids = dec.block_ids.clone()
+    dmsa = time_calls(dec.decode, l2_flush, stream, reps)
+    smsa = time_calls(dec.select_blocks, l2_flush, stream, reps)
+    amsa = time_calls(lambda: dec.sparse_attn(ids), l2_flush, stream, reps)
+    rows = np.diff(wl.q_indptr)
+    sb = bm.step_bytes(wl.context_lens, rows, ids.cpu().numpy())
+    d = spread(dmsa)
+    step_s = d["mean_us"] * 1e-6
+    out = {"decode": d, "select_us": spread(smsa)["mean_us"], "attention_us": spread(amsa)["mean_us"],
+           "query_rows": int(rows.sum()), "query_rows_per_s": round(float(rows.sum()) / step_s, 1),
+           "step_bytes": sb["total"], "achieved_gbs": round(sb["total"] / step_s / 1e9, 1),
+           "frac": round(sb["total"] / step_s / 1e9 / peak, 4), "reps": reps, "device_error_flags": flags}
+    del dec, wl
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_libmsa(args, rank, world, dist):
     import torch
 
@@ -272,48 +346,43 @@ def run_libmsa(args, rank, world, dist):
     ms_per_step = statistics.mean(step_ms)
     ok_flags = dec.errors()
 
-    # ---- dominant call alone (selection: the index-scan kernel with its block max pool,
-    # then the top-k kernel it chains), same flushing
+    # ---- the calls of the step alone, same flushing: the selection (the index-scan kernel
+    # with its block max pool, then the top-k kernel it chains), the exact-score selection
+    # and the sparse attention on the step's block ids
     kr = min(args.steps, 200)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
-    for i in range(kr):
-        l2_flush()
-        evs[i][0].record(stream)
-        dec.select_blocks()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    sel_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    sel_ms = statistics.mean(time_calls(dec.select_blocks, l2_flush, stream, kr))
     ids_now = dec.block_ids.clone()
-    # the exact-score selection (msa_select_blocks_exact), same flushing
-    evx = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
-    for i in range(kr):
-        l2_flush()
-        evx[i][0].record(stream)
-        dec.select_blocks_exact()
-        evx[i][1].record(stream)
-    torch.cuda.synchronize()
-    selx_ms = statistics.mean(a.elapsed_time(b) for a, b in evx)
+    selx_ms = statistics.mean(time_calls(dec.select_blocks_exact, l2_flush, stream, kr))
     dec.block_ids.copy_(ids_now)
-    eva = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(kr)]
-    for i in range(kr):
-        l2_flush()
-        eva[i][0].record(stream)
-        dec.sparse_attn(ids_now)
-        eva[i][1].record(stream)
-    torch.cuda.synchronize()
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in eva)
+    attn_ms = statistics.mean(time_calls(lambda: dec.sparse_attn(ids_now), l2_flush, stream, kr))
 
     kv_insert = measure_kv_insert(l2_flush, stream, reps=min(args.steps, 50))
 
     sel_bytes = bm.select_bytes(wl.context_lens, np.diff(wl.q_indptr))
     step_bytes = bm.step_bytes(wl.context_lens, np.diff(wl.q_indptr), ids_now.cpu().numpy())
     peak, peak_kind = measured_peaks()
-    achieved = sel_bytes / (sel_ms * 1e-3) / 1e9
+    achieved = step_bytes["total"] / (ms_per_step * 1e-3) / 1e9
+    sel_achieved = sel_bytes / (sel_ms * 1e-3) / 1e9
+    traffic = [profile_traffic(k, args.workload) for k in ("select_kernel", "attn_kernel")]
     roofline = {"bound": "hbm",
-                "kernel": "msa_select_blocks = select_kernel (index scan + block max pool) + topk_kernel (chained)",
+                "kernel": "msa_decode = select_kernel (index scan + block max pool) -> topk_kernel -> attn_kernel, "
+                          "chained by programmatic dependent launch",
                 "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profile_traffic("select_kernel", args.workload),
-                "algorithmic_bytes_per_launch": sel_bytes, "avg_launch_us": round(sel_ms * 1e3, 2)}
+                "frac": round(achieved / peak, 4),
+                "traffic": (traffic[0] + traffic[1]) if None not in traffic else None,
+                "algorithmic_bytes_per_launch": step_bytes["total"], "avg_launch_us": round(ms_per_step * 1e3, 2),
+                "selection": {"kernel": "msa_select_blocks = select_kernel + topk_kernel (chained)",
+                              "achieved": round(sel_achieved, 1), "frac": round(sel_achieved / peak, 4),
+                              "traffic": traffic[0], "algorithmic_bytes_per_launch": sel_bytes,
+                              "avg_launch_us": round(sel_ms * 1e3, 2)}}
+
+    # ---- the other workload shapes (their parity is tested; here their device times)
+    presets = {}
+    if not args.no_presets:
+        from block_sparse_attention_nvfp4_gb300 import synth as _synth
+        for name in _synth.PRESETS:
+            if name != args.workload:
+                presets[name] = measure_preset(name, l2_flush, stream, min(args.steps, 30), peak)
 
     # ---- end to end through the public API: a step from pinned host memory (HostIO: the
     # inputs packed into one buffer, one host-to-device copy, the decode, one
@@ -338,17 +407,29 @@ def run_libmsa(args, rank, world, dist):
                    + (", replayed as one CUDA graph" if io.graph is not None else
                       f" (eager: graph capture failed: {io.graph_error})")}
 
-    # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample
+    # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample, at all the
+    # host's cores (OpenMP over requests) and at one core
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         reqs = list(range(min(wl.num_reqs, 16)))
+        srows = int(sum(int(wl.q_indptr[b + 1] - wl.q_indptr[b]) for b in reqs))
+        all_cores = oracle.num_threads()
         t0 = time.perf_counter()
         oracle.decode(wl, reqs)
         dt = time.perf_counter() - t0
-        srows = int(sum(int(wl.q_indptr[b + 1] - wl.q_indptr[b]) for b in reqs))
-        cpu = {"value": round(srows / dt, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+        oracle.set_threads(1)
+        one = reqs[:1]
+        r1 = int(wl.q_indptr[one[0] + 1] - wl.q_indptr[one[0]])
+        t1 = time.perf_counter()
+        oracle.decode(wl, one)
+        dt1 = time.perf_counter() - t1
+        oracle.set_threads(all_cores)
+        cpu = {"value": round(srows / dt, 3), "unit": UNIT, "cores": all_cores, "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{len(reqs)} of {wl.num_reqs} requests of the same workload ({srows} query rows), "
-                         f"one pass, {dt:.2f} s wall"}
+                         f"one pass, {dt:.2f} s wall, OpenMP over requests",
+               "one_core": {"value": round(r1 / dt1, 3), "unit": UNIT, "cores": 1,
+                            "sample": f"1 request ({r1} query rows), {dt1:.2f} s wall"}}
 
     clocks = sampler.summary()
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -356,7 +437,7 @@ def run_libmsa(args, rank, world, dist):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": dict(workload_config(args.workload, spec, "flushed before every timed step (512 MiB write, then read back)"),
                            parallelism=f"replicas x{world}"),
-            "hbm_gbs_step": round(step_bytes["total"] / (ms_per_step * 1e-3) / 1e9, 1),
+            "step_time": spread(step_ms),
             "step_bytes": step_bytes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 3 * args.steps,  # per step: index scan, top-k, sparse attention
             "kernels_us": {"decode": round(ms_per_step * 1e3, 2), "select": round(sel_ms * 1e3, 2),
@@ -368,6 +449,7 @@ def run_libmsa(args, rank, world, dist):
                              "what": "msa_select_blocks_exact: the same selection with exact index scores "
                                      "(FP16 tiles and MMAs), timed alone like the roofline call"},
             "kv_insert_nvfp4": kv_insert,
+            "workloads": presets,
             "clocks": clocks, "timed_wall_s": round(wall, 4), "device_error_flags": ok_flags,
             "impl": "libmsa"}
     return line
@@ -375,48 +457,49 @@ def run_libmsa(args, rank, world, dist):
 
 # ----------------------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
+    """The oracle as it stands, on the host cores (OpenMP over requests), on the same
+    workload. A step is the whole batch when K + W such steps fit the time budget;
+    otherwise each step is a bounded sample of it (an equal share of requests, so every
+    core still has work), and the line says so."""
     import oracle
     from block_sparse_attention_nvfp4_gb300 import synth
 
     spec = synth.preset(args.workload)
     wl = synth.make_workload(spec)
     oracle.build()
-    # per step: one request of the workload through the whole oracle path; if K+W
-    # such steps would exceed the time budget, a step takes one query row's share
-    t0 = time.perf_counter()
-    oracle.decode(wl, [0])
-    one = time.perf_counter() - t0
+    cores = oracle.num_threads()
     budget = 240.0
-    reqs_per_step = 1
-    rows_per_req = int(wl.q_indptr[1] - wl.q_indptr[0])
     steps_total = args.steps + args.warmup
-    note = "one request per step (all its query rows), full path"
-    for i in range(args.warmup):
-        oracle.decode(wl, [i % wl.num_reqs])
-    times = []
-    projected = steps_total * one
-    if projected > budget:
-        # bounded: time one request per (budget / one) steps and spread it evenly
-        per = max(1, int(math.ceil(projected / budget)))
-        note = f"one request every {per} steps (time spread over those steps): budget {budget:.0f} s"
+    # probe: one pass over one request per core
+    probe = list(range(min(wl.num_reqs, cores)))
+    t0 = time.perf_counter()
+    oracle.decode(wl, probe)
+    per_wave = time.perf_counter() - t0                  # one request per core, all cores busy
+    waves = math.ceil(wl.num_reqs / cores)
+    if steps_total * waves * per_wave <= budget:
+        per_step = list(range(wl.num_reqs))
+        note = f"the whole batch per step ({wl.num_reqs} requests on {cores} threads)"
     else:
-        per = 1
+        n = max(1, min(wl.num_reqs, int(budget / (steps_total * per_wave)) * cores or 1))
+        per_step = list(range(n))
+        note = (f"{n} of {wl.num_reqs} requests per step (the whole batch would take "
+                f"{waves * per_wave:.1f} s a step; budget {budget:.0f} s for {steps_total} steps)")
+    rows_per_step = int(sum(int(wl.q_indptr[b + 1] - wl.q_indptr[b]) for b in per_step))
+    for _ in range(args.warmup):
+        oracle.decode(wl, per_step)
     total = 0.0
-    units = 0.0
-    for i in range(args.steps):
-        if i % per == 0:
-            t0 = time.perf_counter()
-            oracle.decode(wl, [i % wl.num_reqs])
-            total += time.perf_counter() - t0
-            units += rows_per_req * reqs_per_step
-    value = units / total
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(wl, per_step)
+        total += time.perf_counter() - t0
+    value = rows_per_step * args.steps / total
     return {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(1e3 * total / max(1, args.steps // per), 3),
+            "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(workload_config(args.workload, spec, "n/a (host)"), parallelism="host cores"),
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": note},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": min(cores, len(per_step)),
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": note},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -428,6 +511,7 @@ def main():
     ap.add_argument("--impl", default="libmsa", choices=["libmsa", "reference"])
     ap.add_argument("--workload", default="spec8_128k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-presets", action="store_true", help="skip the other workload shapes' figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -25,7 +25,8 @@ FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS, FLAG_BAD_SLOT = 0x1,
 # symbols include/msa.h declares (checked by the CPU tests)
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
-           "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact")
+           "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact",
+           "msa_select_blocks_noalloc_get_error")
 
 
 class MSAError(RuntimeError):
@@ -81,6 +82,7 @@ def load(path: str = LIB_PATH):
             lib.msa_select_blocks.argtypes = [ap, vp, vp, vp, sz, vp]
             lib.msa_select_blocks_exact.argtypes = [ap, vp, vp, vp, sz, vp]
             lib.msa_select_blocks_noalloc.argtypes = [ap, vp, vp, vp]
+            lib.msa_select_blocks_noalloc_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.msa_sparse_attn_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_dequant_rows.argtypes = [vp, vp, i64, vp, ctypes.c_int32, vp]
@@ -179,6 +181,16 @@ def msa_select_blocks_noalloc(args: Args, block_ids: torch.Tensor, block_scores:
     see include/msa.h for the size limit and the sharing rules)."""
     _check(load().msa_select_blocks_noalloc(ctypes.byref(args), _ptr(block_ids), _ptr(block_scores),
                                             _stream(stream)), "msa_select_blocks_noalloc")
+
+
+def msa_select_blocks_noalloc_get_error(stream=None) -> int:
+    """Device error flags (MSA_FLAG_*) of the most recent msa_select_blocks_noalloc call
+    (synchronises the stream)."""
+    flags = ctypes.c_uint32(0)
+    code = load().msa_select_blocks_noalloc_get_error(_stream(stream), ctypes.byref(flags))
+    if code not in (MSA_OK, -5, -6):
+        _check(code, "msa_select_blocks_noalloc_get_error")
+    return int(flags.value)
 
 
 def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],

@@ -67,6 +67,8 @@ cudaError_t get_encode_fn() {
   return cudaSuccess;
 }
 
+}  // namespace
+
 // 2-D view of an NVFP4 code plane [rows][64 bytes], boxes of 128 rows, 64-byte swizzle.
 msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows) {
   if (get_encode_fn() != cudaSuccess) return MSA_ERR_CUDA;
@@ -80,7 +82,11 @@ msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows
   return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
 }
 
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
 
 // Host-side checks of everything the host can see. Device-visible values
 // (lengths, page ids) are checked by the kernels.
@@ -112,11 +118,15 @@ msa_status validate(const msa_decode_args* a, bool need_kv, bool need_idx) {
   return MSA_OK;
 }
 
-msa_status check_device(DeviceInfo* d) {
-  if (device_info(d) != cudaSuccess) return MSA_ERR_CUDA;
-  if (d->major != 10 || d->minor != 3) return MSA_ERR_UNSUPPORTED;
+msa_status check_device(int* sm_count) {
+  DeviceInfo d;
+  if (device_info(&d) != cudaSuccess) return MSA_ERR_CUDA;
+  if (d.major != 10 || d.minor != 3) return MSA_ERR_UNSUPPORTED;
+  *sm_count = d.sm_count;
   return MSA_OK;
 }
+
+namespace {
 
 struct Ws {
   uint32_t* flags;
@@ -137,25 +147,6 @@ msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, const Plan
   w->part_o = reinterpret_cast<float*>(base + L.part_o);
   w->part_lse2 = reinterpret_cast<float*>(base + L.part_lse2);
   return MSA_OK;
-}
-
-SelectParams select_params(const msa_decode_args* a, const Ws& w, int32_t* ids, float* scores_out) {
-  SelectParams p = {};
-  p.num_reqs = a->num_reqs;
-  p.num_pages = a->num_pages;
-  p.max_pages = a->max_pages_per_req;
-  p.total_rows = a->total_rows;
-  p.context_lens = a->context_lens;
-  p.q_indptr = a->q_indptr;
-  p.block_table = a->block_table;
-  p.q_idx = a->q_idx;
-  p.ki_scale = a->ki_scale;
-  p.block_S = w.block_S;
-  p.s_stride = score_stride(a->max_pages_per_req);
-  p.flags = w.flags;
-  p.block_ids = ids;
-  p.block_scores_out = scores_out;
-  return p;
 }
 
 AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, const int32_t* ids, uint16_t* out,
@@ -228,6 +219,37 @@ WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_p
   return L;
 }
 
+msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
+                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st) {
+  // the scan's shared memory grows with the request count (its page prefix); the exact-score
+  // layout leaves room for about 560 requests within the 227 KB a CTA may opt into
+  if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
+  if (args->num_reqs == 0) return MSA_OK;
+  CUtensorMap map;
+  msa_status s = encode_code_map(&map, args->ki_data, static_cast<long long>(args->num_pages) * kBlock);
+  if (s != MSA_OK) return s;
+  SelectParams p = {};
+  p.num_reqs = args->num_reqs;
+  p.num_pages = args->num_pages;
+  p.max_pages = args->max_pages_per_req;
+  p.total_rows = args->total_rows;
+  p.context_lens = args->context_lens;
+  p.q_indptr = args->q_indptr;
+  p.block_table = args->block_table;
+  p.q_idx = args->q_idx;
+  p.ki_scale = args->ki_scale;
+  p.block_S = block_S;
+  p.s_stride = score_stride(args->max_pages_per_req);
+  p.flags = flags;
+  p.block_ids = ids;
+  p.block_scores_out = scores_out;
+  p.token_scores = tok;
+  p.score_stride = stride;
+  if (launch_select(map, p, mode, sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (mode != 1 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -278,24 +300,14 @@ msa_status msa_get_error(void* ws, size_t ws_bytes, void* stream, uint32_t* flag
 
 static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
                              long long stride, void* ws, size_t ws_bytes, cudaStream_t st) {
-  DeviceInfo d;
-  msa_status s = check_device(&d);
+  int sms = 0;
+  msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
-  // the scan's shared memory grows with the request count (its page prefix); the exact-score
-  // layout leaves room for about 560 requests within the 227 KB a CTA may opt into
   if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
-  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  const Plan plan = make_plan(args->num_reqs, sms);
   Ws w;
   if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
-  if (args->num_reqs == 0) return MSA_OK;
-  CUtensorMap map;
-  if ((s = encode_code_map(&map, args->ki_data, static_cast<long long>(args->num_pages) * kBlock)) != MSA_OK) return s;
-  SelectParams p = select_params(args, w, ids, scores_out);
-  p.token_scores = tok;
-  p.score_stride = stride;
-  if (launch_select(map, p, mode, d.sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
-  if (mode != 1 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
-  return MSA_OK;
+  return launch_selection(args, mode, ids, scores_out, tok, stride, w.flags, w.block_S, sms, st);
 }
 
 msa_status msa_index_scores(const msa_decode_args* args, float* scores, int64_t score_stride, void* ws,
@@ -330,9 +342,9 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
   if (scores == nullptr || block_ids == nullptr ||
       score_stride < static_cast<int64_t>(args->max_pages_per_req) * kBlock)
     return MSA_ERR_INVALID_ARG;
-  DeviceInfo d;
-  if ((s = check_device(&d)) != MSA_OK) return s;
-  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  int sms = 0;
+  if ((s = check_device(&sms)) != MSA_OK) return s;
+  const Plan plan = make_plan(args->num_reqs, sms);
   Ws w;
   if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
   if (args->num_reqs == 0) return MSA_OK;
@@ -354,10 +366,10 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
 
 static msa_status run_attn(const msa_decode_args* args, const int32_t* ids, uint16_t* out, float* lse, void* ws,
                            size_t ws_bytes, cudaStream_t st, bool pdl) {
-  DeviceInfo d;
-  msa_status s = check_device(&d);
+  int sms = 0;
+  msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
-  const Plan plan = make_plan(args->num_reqs, d.sm_count);
+  const Plan plan = make_plan(args->num_reqs, sms);
   Ws w;
   if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
   if (args->num_reqs == 0) return MSA_OK;
@@ -389,8 +401,8 @@ msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t
     return MSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(codes) & 3u) != 0 || (reinterpret_cast<uintptr_t>(out_e4m3) & 3u) != 0)
     return MSA_ERR_INVALID_ARG;
-  DeviceInfo d;
-  msa_status s = check_device(&d);
+  int sms = 0;
+  msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
   if (nrows == 0) return MSA_OK;
   return launch_dequant_rows(codes, scales, nrows, out_e4m3, path, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -408,8 +420,8 @@ msa_status msa_kv_insert_nvfp4(const msa_kv_insert_args* a, void* ws, size_t ws_
     return MSA_ERR_INVALID_ARG;
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0 || ws_bytes < kWsAlign)
     return MSA_ERR_WORKSPACE;
-  DeviceInfo d;
-  msa_status s = check_device(&d);
+  int sms = 0;
+  msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
   if (a->num_tokens == 0 || (a->k == nullptr && a->v == nullptr && a->k_idx == nullptr)) return MSA_OK;
   KvInsertParams p;
@@ -426,7 +438,7 @@ msa_status msa_kv_insert_nvfp4(const msa_kv_insert_args* a, void* ws, size_t ws_
   p.ki_data = a->ki_data;
   p.ki_scale = a->ki_scale;
   p.flags = static_cast<uint32_t*>(ws);
-  return launch_kv_insert(p, d.sm_count, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return launch_kv_insert(p, sms, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -330,9 +330,10 @@ __device__ __forceinline__ void dq8_signed(uint32_t w, uint32_t L0, uint32_t L1,
 //
 // Ranking key: the score's order-preserving integer image in the high word and
 // the complemented block id in the low word, so larger key = higher score, then
-// lower id; NaN ranks below everything.
+// lower id; NaN ranks below everything. -0.0 and +0.0 are equal scores (they tie,
+// and the lower id wins), so both map to the image of +0.0.
 __device__ __forceinline__ uint64_t topk_key(float v, int id) {
-  uint32_t u = __float_as_uint(v);
+  const uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
   uint32_t hi;
   if (v != v) hi = 0u;
   else hi = (u & 0x80000000u) ? ~u : (u | 0x80000000u);

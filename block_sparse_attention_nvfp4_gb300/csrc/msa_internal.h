@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/msa.h"
+
 namespace msa {
 
 // Fused index scan -> block max pool -> top-k (and the per-token score variant).
@@ -106,5 +108,19 @@ cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
 cudaError_t launch_kv_insert(const KvInsertParams& prm, int sm_count, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,
                                 cudaStream_t st);
+
+// Host-side helpers of the C ABI, shared by the entry points in msa_api.cu and
+// msa_noalloc.cu so that both take the same checks and the same launch sequence.
+// validate: every check the host can make (need_kv / need_idx: the K/V or the
+// index-key operands are used). check_device: the current device is sm_103 (its SM
+// count returned). encode_code_map: the TMA view of an index-key code plane.
+// launch_selection: the scan (mode 0 fused, 1 per-token scores, 2 exact scores) and,
+// for modes 0 and 2, the chained top-k, with the given flags word and block-score
+// scratch ([B][4][score_stride(max_pages)] FP32).
+msa_status validate(const msa_decode_args* a, bool need_kv, bool need_idx);
+msa_status check_device(int* sm_count);
+msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows);
+msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
+                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st);
 
 }  // namespace msa

@@ -174,19 +174,28 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* bl
  * pages have no counterpart to this entry point; it exists for hosts that hand a
  * library only the tensors it works on and keep the allocator to themselves
  * (plugin / custom-operator interfaces), and for decode loops that must not call
- * cudaMalloc because it can synchronise the device. It runs the same kernels as
- * msa_select_blocks with the same outputs, but its scratch (error flags and block
+ * cudaMalloc because it can synchronise the device. It runs the same host checks,
+ * kernels and outputs as msa_select_blocks, but its scratch (error flags and block
  * scores: 256 + 16*B*P4 bytes, where P4 is max_pages_per_req rounded up to a
  * multiple of 4) lives in a fixed 8 MiB device buffer inside the library, which
- * every GPU that loads libmsa holds until the process exits. Batches needing more return
- * MSA_ERR_WORKSPACE before any launch. It allocates nothing: the first call on each
- * device looks the buffer's address up once (make that first call before any
- * stream capture), and every call clears the flags with an async memset on
- * `stream`. All calls share the one buffer, so calls that overlap on the
- * GPU (other streams, other host threads) race and must be serialised by the
- * caller. Device error flags are cleared per call and not reported. */
+ * every GPU that loads libmsa holds until the process exits. Batches needing more
+ * return MSA_ERR_WORKSPACE before any launch. It allocates nothing: each call looks
+ * the buffer's device address up (cudaGetSymbolAddress; the first lookup on a device
+ * may load the library's device code there, so make the first call on each device
+ * before any stream capture), clears the flags with an async memset on `stream` and
+ * launches. All calls share the one buffer, so calls that overlap on the GPU (other
+ * streams, other host threads) race and must be serialised by the caller. The
+ * device error flags of the most recent call are read with
+ * msa_select_blocks_noalloc_get_error. */
 msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int32_t* block_ids, float* block_scores,
                                      void* stream);
+
+/* The device error flags (MSA_FLAG_*) left by the most recent msa_select_blocks_noalloc
+ * call, read from the library's fixed buffer: synchronises `stream`, writes *flags
+ * (host) and returns MSA_OK when none is set, else the matching error code
+ * (MSA_ERR_TIMEOUT, MSA_ERR_BAD_TABLE), as msa_get_error does for a workspace. The
+ * next msa_select_blocks_noalloc call clears them. Allocates nothing. */
+msa_status msa_select_blocks_noalloc_get_error(void* stream, uint32_t* flags);
 
 /* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, three
  * kernels on `stream`, each chained to the one before it with programmatic

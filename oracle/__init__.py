@@ -79,6 +79,8 @@ def _load():
             lib.oracle_attend.argtypes = [ap, ctypes.c_int, ip, dp, dp]
             lib.oracle_decode.argtypes = [ap, ctypes.c_int, ip, ip, dp, dp, dp]
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_threads.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
             u8p = ctypes.POINTER(ctypes.c_uint8)
             fp = ctypes.POINTER(ctypes.c_float)
             lib.oracle_e2m1_round.restype = ctypes.c_int
@@ -242,6 +244,12 @@ def decode(wl, reqs=None):
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_threads(n: int) -> int:
+    """Threads of decode()'s loop over requests (scheduling only; results do not
+    depend on it). Returns the count in effect."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 # ---------------------------------------------------------------- NVFP4 insertion

@@ -463,3 +463,16 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Thread count for the request loop of oracle_decode (host-side scheduling only; it
+ * changes no arithmetic: each request's result is computed by one thread in a fixed
+ * order). n < 1 leaves it unchanged. Returns the count now in effect. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+  return omp_get_max_threads();
+#else
+  (void)n;
+  return 1;
+#endif
+}

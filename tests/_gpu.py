@@ -22,10 +22,11 @@ def assert_out_close(got, ref, what=""):
 
 
 def selection_matches(gpu_ids, ref_ids, S_ref, nb):
-    """True when the GPU's ids equal the oracle's, or differ only where the
-    oracle's 16th and 17th block scores (the 15th/16th best non-recent blocks)
-    lie within TIE_REL relative of each other, with every swapped block inside
-    that near-tie band."""
+    """True when the GPU's ids equal the oracle's, or differ only at a near-tie:
+    the oracle's 16th and 17th block scores (the 15th/16th best non-recent blocks)
+    differ but lie within TIE_REL relative of each other, and every swapped block
+    lies inside that band. An exact tie (equal scores) is never waived: the lower
+    block id must win, as the oracle's rule says."""
     g = sorted(int(x) for x in gpu_ids if x >= 0)
     r = sorted(int(x) for x in ref_ids if x >= 0)
     if g == r:
@@ -34,11 +35,20 @@ def selection_matches(gpu_ids, ref_ids, S_ref, nb):
         return False
     others = np.sort(S_ref[: nb - 1])[::-1]
     s15, s16 = others[14], others[15]
+    if s15 == s16:
+        return False
     band = TIE_REL * max(abs(s15), abs(s16))
     if abs(s15 - s16) > band:
         return False
     swapped = set(g) ^ set(r)
     return all(abs(S_ref[c] - s15) <= 2 * band or abs(S_ref[c] - s16) <= 2 * band for c in swapped)
+
+
+def assert_topk_exact_on_own_scores(ids, block_scores, nb, what=""):
+    """The top-k given the GPU's own FP32 block scores is exact: the ids equal the
+    oracle's selection (full sort, ties to the lower id) run on those same scores."""
+    want = oracle.select(np.asarray(block_scores[:nb], dtype=np.float32).astype(np.float64))
+    assert np.array_equal(np.asarray(ids), want), (what, ids, want)
 
 
 def check_decode(wl, reqs=None, dec=None):

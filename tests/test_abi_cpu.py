@@ -59,7 +59,12 @@ def test_host_validation_rejects_before_any_cuda_call(lib, field, value, code):
     a = _args()
     setattr(a, field, value)
     n = ctypes.c_size_t(0)
-    assert lib.msa_workspace_size(ctypes.byref(a), ctypes.byref(n)) == (code if field != "q" else lib.msa_workspace_size(ctypes.byref(a), ctypes.byref(n)))
+    ws_rc = lib.msa_workspace_size(ctypes.byref(a), ctypes.byref(n))
+    if field == "q":
+        # the workspace size depends on the batch's sizes only, not on its data pointers
+        assert ws_rc != -1
+    else:
+        assert ws_rc == code
     rc = lib.msa_decode(ctypes.byref(a), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000), None,
                         ctypes.c_void_p(0x40000), 1 << 20, None)
     assert rc == code

@@ -61,21 +61,22 @@ def test_exact_selection_matches_oracle():
     assert differ > 0, "the exact and the E4M3 selections gave identical block scores"
 
 
-def test_exact_selection_full_size_sampled():
-    """The benchmark's shape (16 x 131,072 tokens x 8 rows); two requests checked against
-    the oracle's exact mode, the others' ids for validity."""
+def test_exact_selection_full_size():
+    """The benchmark's shape (16 x 131,072 tokens x 8 rows); every request checked against
+    the oracle's exact mode, and the top-k exact on the GPU's own block scores."""
     wl = synth.make_workload(synth.preset("spec8_128k"))
     dec = _gpu.decoder(wl, with_block_scores=True)
     ids = dec.select_blocks_exact().cpu().numpy()
     bs = dec.block_scores.cpu().numpy()
     torch.cuda.synchronize()
     assert dec.errors() == 0
-    for b in (0, 9):
+    for b in range(wl.num_reqs):
         nb = (int(wl.context_lens[b]) + 127) // 128
         Sr = oracle.block_scores(wl, b, exact=True)
         np.testing.assert_allclose(bs[b, :, :nb], Sr, rtol=1e-5, atol=1e-4)
         for g in range(4):
             assert _gpu.selection_matches(ids[b, g], oracle.select(Sr[g]), Sr[g], nb), (b, g)
+            _gpu.assert_topk_exact_on_own_scores(ids[b, g], bs[b, g], nb, (b, g))
     for b in range(wl.num_reqs):
         nb = (int(wl.context_lens[b]) + 127) // 128
         for g in range(4):
