@@ -130,22 +130,16 @@ namespace {
 
 struct Ws {
   uint32_t* flags;
-  uint32_t* pair_cnt;
   float* block_S;
-  float* part_o;
-  float* part_lse2;
 };
 
-msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, const Plan& plan, Ws* w) {
+msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, Ws* w) {
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0) return MSA_ERR_WORKSPACE;
-  const WsLayout L = ws_layout(a->num_reqs, a->total_rows, a->max_rows_per_req, a->max_pages_per_req, plan);
+  const WsLayout L = ws_layout(a->num_reqs, a->max_pages_per_req);
   if (ws_bytes < L.total) return MSA_ERR_WORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(ws);
   w->flags = reinterpret_cast<uint32_t*>(base + L.flags);
-  w->pair_cnt = reinterpret_cast<uint32_t*>(base + L.pair_cnt);
   w->block_S = reinterpret_cast<float*>(base + L.block_S);
-  w->part_o = reinterpret_cast<float*>(base + L.part_o);
-  w->part_lse2 = reinterpret_cast<float*>(base + L.part_lse2);
   return MSA_OK;
 }
 
@@ -168,10 +162,8 @@ AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, 
   p.sm_scale_log2 = a->sm_scale * 1.4426950408889634f;
   p.blocks_per_split = plan.blocks_per_split;
   p.splits = plan.splits;
+  p.copies = plan.copies;
   p.max_m = kQPerKV * a->max_rows_per_req;
-  p.part_o = w.part_o;
-  p.part_lse2 = w.part_lse2;
-  p.pair_cnt = w.pair_cnt;
   p.flags = w.flags;
   p.out = out;
   p.lse = lse;
@@ -182,13 +174,11 @@ AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, 
 
 int score_stride(int max_pages) { return (max_pages + 3) / 4 * 4; }
 
-Plan make_plan(int num_reqs, int sm_count) {
+Plan make_plan(int num_reqs, int max_rows_per_req, int sm_count) {
   Plan pl;
-  // one attention CTA per SM: the fewest blocks per split that fit the (request,
-  // group) x split grid into one wave, but at least 2: the last CTA's merge reads the
-  // partials two splits per round trip, so with few (request, group) pairs (one long
-  // request) 16 one-block splits cost more in merging than they save (measured on
-  // GB300: 1 x 524,288 tokens x 4 rows, attention 22.5 -> 20.5 us)
+  // one attention CTA per SM: the fewest blocks per split that fit the (request, group)
+  // x split grid into one wave, but at least 2, so a (request, group)'s splits form a
+  // cluster of at most 8 CTAs (the portable cluster size) that merges its partials
   const int pairs = num_reqs * kGroups;
   const int target = sm_count > 0 ? sm_count : 1;
   int bps = pairs > 0 ? pow2_ceil((kTopK * pairs + target - 1) / target) : kTopK;
@@ -196,25 +186,19 @@ Plan make_plan(int num_reqs, int sm_count) {
   if (bps > kTopK) bps = kTopK;
   pl.blocks_per_split = bps;
   pl.splits = kTopK / bps;
+  // 4 copies of the <= 32 query rows down the 128-row tile when every request has at most
+  // 4 rows (each thread then takes 32 keys of a block), else 2 copies of <= 64 rows
+  pl.copies = max_rows_per_req <= 4 ? 4 : 2;
   return pl;
 }
 
-WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan) {
+WsLayout ws_layout(int num_reqs, int max_pages) {
   WsLayout L;
-  (void)total_rows;
   size_t off = 0;
   L.flags = off;
   off = align_up(off + 16);
-  L.pair_cnt = off;
-  off = align_up(off + sizeof(uint32_t) * static_cast<size_t>(num_reqs) * kGroups);
   L.block_S = off;
   off = align_up(off + sizeof(float) * static_cast<size_t>(num_reqs) * kGroups * score_stride(max_pages));
-  const size_t m = static_cast<size_t>(kQPerKV) * max_rows_per_req;
-  const size_t parts = plan.splits > 1 ? static_cast<size_t>(plan.splits) * num_reqs * kGroups * m : 0;
-  L.part_o = off;
-  off = align_up(off + sizeof(float) * parts * kDim);
-  L.part_lse2 = off;
-  off = align_up(off + sizeof(float) * parts);
   L.total = off;
   return L;
 }
@@ -275,8 +259,8 @@ msa_status msa_workspace_size(const msa_decode_args* args, size_t* bytes) {
   if (st != MSA_OK) return st;
   DeviceInfo d;
   if (device_info(&d) != cudaSuccess) return MSA_ERR_CUDA;
-  const Plan plan = make_plan(args->num_reqs, d.sm_count);
-  *bytes = ws_layout(args->num_reqs, args->total_rows, args->max_rows_per_req, args->max_pages_per_req, plan).total;
+  (void)d;
+  *bytes = ws_layout(args->num_reqs, args->max_pages_per_req).total;
   return MSA_OK;
 }
 
@@ -304,9 +288,8 @@ static msa_status run_select(const msa_decode_args* args, int mode, int32_t* ids
   msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
   if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
-  const Plan plan = make_plan(args->num_reqs, sms);
   Ws w;
-  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
   return launch_selection(args, mode, ids, scores_out, tok, stride, w.flags, w.block_S, sms, st);
 }
 
@@ -344,9 +327,8 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
     return MSA_ERR_INVALID_ARG;
   int sms = 0;
   if ((s = check_device(&sms)) != MSA_OK) return s;
-  const Plan plan = make_plan(args->num_reqs, sms);
   Ws w;
-  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
   if (args->num_reqs == 0) return MSA_OK;
   MaxpoolParams p = {};
   p.num_reqs = args->num_reqs;
@@ -369,12 +351,17 @@ static msa_status run_attn(const msa_decode_args* args, const int32_t* ids, uint
   int sms = 0;
   msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
-  const Plan plan = make_plan(args->num_reqs, sms);
+  const Plan plan = make_plan(args->num_reqs, args->max_rows_per_req, sms);
   Ws w;
-  if ((s = carve(args, ws, ws_bytes, plan, &w)) != MSA_OK) return s;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
   if (args->num_reqs == 0) return MSA_OK;
+  // the K and V code planes as [num_pages * 4 * 128 rows][64 bytes] for the tensor copies
+  const long long rows = static_cast<long long>(args->num_pages) * kGroups * kBlock;
+  CUtensorMap kmap, vmap;
+  if ((s = encode_code_map(&kmap, args->k_data, rows)) != MSA_OK) return s;
+  if ((s = encode_code_map(&vmap, args->v_data, rows)) != MSA_OK) return s;
   AttnParams p = attn_params(args, w, plan, ids, out, lse);
-  return launch_attn(p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+  return launch_attn(kmap, vmap, p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* block_ids, uint16_t* out_bf16,

@@ -40,7 +40,8 @@ struct MaxpoolParams {
   uint32_t* flags;
 };
 
-// Sparse attention over selected blocks, split across CTAs, merged by the last arriver.
+// Sparse attention over selected blocks, split across the CTAs of a thread-block
+// cluster that merges its partials through distributed shared memory.
 struct AttnParams {
   int num_reqs, num_pages, max_pages, total_rows;
   const int32_t* context_lens;
@@ -48,17 +49,15 @@ struct AttnParams {
   const int32_t* block_table;
   const int32_t* block_ids;  // [B][4][16]
   const uint8_t* q;
-  const uint8_t* k_data;
+  const uint8_t* k_data;     // codes also read through tensor maps (launch_attn)
   const uint8_t* k_scale;
   const uint8_t* v_data;
   const uint8_t* v_scale;
   float sm_scale_log2;       // sm_scale * log2(e)
   int blocks_per_split;
-  int splits;
+  int splits;                // CTAs per (request, group) = cluster size, 1..8
+  int copies;                // query-row copies down the MMA tile: 2, or 4 when rows <= 4
   int max_m;                 // 8 * max_rows_per_req
-  float* part_o;             // workspace [splits][B*4][max_m][128]
-  float* part_lse2;          // workspace [splits][B*4][max_m] (log2 domain)
-  uint32_t* pair_cnt;        // workspace [B*4]
   uint32_t* flags;
   uint16_t* out;             // [rows][32][128] bf16 bits
   float* lse;                // optional [rows][32]
@@ -83,17 +82,18 @@ struct KvInsertParams {
 
 // Workspace layout, offsets in bytes (each 256-aligned).
 struct WsLayout {
-  size_t flags, pair_cnt, block_S, part_o, part_lse2, total;
+  size_t flags, block_S, total;
 };
 
 struct Plan {
   int blocks_per_split;   // attention
   int splits;
+  int copies;
 };
 
-Plan make_plan(int num_reqs, int sm_count);
+Plan make_plan(int num_reqs, int max_rows_per_req, int sm_count);
 int score_stride(int max_pages);  // block-score row length: max_pages rounded up to 4
-WsLayout ws_layout(int num_reqs, int total_rows, int max_rows_per_req, int max_pages, const Plan& plan);
+WsLayout ws_layout(int num_reqs, int max_pages);
 
 size_t select_smem_bytes(int num_reqs, int mode);  // mode 2: the exact-score layout
 size_t attn_smem_bytes();
@@ -104,7 +104,9 @@ cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, in
 // to the scan with programmatic dependent launch
 cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st);
 cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
-cudaError_t launch_attn(const AttnParams& prm, bool pdl, cudaStream_t st);
+// kmap / vmap: tensor maps of the K and V code planes (encode_code_map over num_pages * 4 * 128 rows)
+cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& prm, bool pdl,
+                        cudaStream_t st);
 cudaError_t launch_kv_insert(const KvInsertParams& prm, int sm_count, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,
                                 cudaStream_t st);

@@ -162,12 +162,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t
   return mbar_try(bar, parity) || mbar_wait(bar, parity, flags);
 }
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float m;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
-  return m;
-}
-
 // Maximum over the visible columns n <= lim of 32 scores starting at column n0.
 __device__ __forceinline__ float max32_masked(const uint32_t (&v)[32], int n0, int lim) {
   float m = -INFINITY;
