@@ -143,7 +143,7 @@ msa_status carve(const msa_decode_args* a, void* ws, size_t ws_bytes, Ws* w) {
   return MSA_OK;
 }
 
-AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, const int32_t* ids, uint16_t* out,
+AttnParams attn_params(const msa_decode_args* a, const Ws& w, const Plan& plan, int32_t* ids, uint16_t* out,
                        float* lse) {
   AttnParams p = {};
   p.num_reqs = a->num_reqs;
@@ -204,7 +204,8 @@ WsLayout ws_layout(int num_reqs, int max_pages) {
 }
 
 msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
-                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st) {
+                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st,
+                            bool with_topk) {
   // the scan's shared memory grows with the request count (its page prefix); the exact-score
   // layout leaves room for about 560 requests within the 227 KB a CTA may opt into
   if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
@@ -230,7 +231,7 @@ msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids,
   p.token_scores = tok;
   p.score_stride = stride;
   if (launch_select(map, p, mode, sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
-  if (mode != 1 && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (mode != 1 && with_topk && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }
 
@@ -346,8 +347,10 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
   return launch_maxpool_topk(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
-static msa_status run_attn(const msa_decode_args* args, const int32_t* ids, uint16_t* out, float* lse, void* ws,
-                           size_t ws_bytes, cudaStream_t st, bool pdl) {
+// fused: the attention kernel selects the ids itself from the block scores the scan left in
+// the workspace (and writes them to ids); otherwise it reads the given ids
+static msa_status run_attn(const msa_decode_args* args, int32_t* ids, uint16_t* out, float* lse, void* ws,
+                           size_t ws_bytes, cudaStream_t st, bool pdl, bool fused) {
   int sms = 0;
   msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
@@ -361,6 +364,10 @@ static msa_status run_attn(const msa_decode_args* args, const int32_t* ids, uint
   if ((s = encode_code_map(&kmap, args->k_data, rows)) != MSA_OK) return s;
   if ((s = encode_code_map(&vmap, args->v_data, rows)) != MSA_OK) return s;
   AttnParams p = attn_params(args, w, plan, ids, out, lse);
+  if (fused) {
+    p.block_S = w.block_S;
+    p.s_stride = score_stride(args->max_pages_per_req);
+  }
   return launch_attn(kmap, vmap, p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
@@ -369,7 +376,8 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* bl
   msa_status s = validate(args, true, false);
   if (s != MSA_OK) return s;
   if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
-  return run_attn(args, block_ids, out_bf16, lse, ws, ws_bytes, static_cast<cudaStream_t>(stream), false);
+  return run_attn(args, const_cast<int32_t*>(block_ids), out_bf16, lse, ws, ws_bytes,
+                  static_cast<cudaStream_t>(stream), false, false);
 }
 
 msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse, void* ws,
@@ -378,8 +386,24 @@ msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t*
   if (s != MSA_OK) return s;
   if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((s = run_select(args, 0, block_ids, nullptr, nullptr, 0, ws, ws_bytes, st)) != MSA_OK) return s;
-  return run_attn(args, block_ids, out_bf16, lse, ws, ws_bytes, st, true);
+  int sms = 0;
+  if ((s = check_device(&sms)) != MSA_OK) return s;
+  if (select_smem_bytes(args->num_reqs, 0) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
+  // the index scan with its block max pool, then the attention, chained by programmatic
+  // dependent launch. The top-k runs in a kernel of its own between them (one CTA per
+  // request), except when requests may exceed 1,025 blocks and the attention splits each
+  // (request, group) over 4 or more CTAs: then each CTA of the (request, group)'s cluster
+  // ranks a share of the candidates inside the attention kernel and the cluster merges the
+  // shares (measured on GB300: one 524,288-token request 45.5 -> 42-43 us per step; batches
+  // with one or two splits, e.g. 16 x 131,072 or 64 ragged requests, are faster with the kernel)
+  const Plan plan = make_plan(args->num_reqs, args->max_rows_per_req, sms);
+  const bool fused_topk = args->max_pages_per_req > 1025 && plan.splits >= 4;
+  if ((s = launch_selection(args, 0, block_ids, nullptr, nullptr, 0, w.flags, w.block_S, sms, st, !fused_topk)) !=
+      MSA_OK)
+    return s;
+  return run_attn(args, block_ids, out_bf16, lse, ws, ws_bytes, st, true, fused_topk);
 }
 
 msa_status msa_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t nrows, uint8_t* out_e4m3,

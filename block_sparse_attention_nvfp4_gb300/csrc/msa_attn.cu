@@ -106,6 +106,7 @@ struct AttnSmem {
   uint64_t s_full[kSets], p_full[kSets], pv_done[kSets], o_final[kSets], mma_drain[1 + kSets];
   float xm[128], xl[128];                           // set 1's reference max and sum per TMEM lane
   int stage_bad[kAttnStages];
+  uint64_t tk_local[kTopK];                         // this CTA's 15 best candidates (the cluster reads them)
   int ids[kTopK];
   int phys[kTopK];                                  // block-table entries of the selected blocks
   uint32_t taddr;
@@ -176,6 +177,149 @@ __device__ __forceinline__ void dq_chunk_v(uint32_t lut_t, const uint4& v, uint3
                  h[4 * cc + 3]);
 }
 
+// Scratch of the fused top-k (in the first K tile, free until block 0 is dequantised).
+struct TopkScratch {
+  uint64_t lm[128];        // the four warps' per-thread maximum keys
+  uint64_t tq[4];          // per-warp threshold candidates
+  uint64_t surv[64];       // candidates at or above the threshold
+  uint64_t all[8][kTopK];  // the cluster's lists, gathered by warp 0
+  int cnt;
+};
+
+// The 15 best candidates c in [lo, hi) of one group's block scores S (ranking keys: score,
+// then lower id), descending, into out[0..14] (0 where there are fewer), by the 128 threads
+// t = 0..127 of warps 0..3 (named barrier 2). Same threshold idea as the top-k kernel: T =
+// the largest per-thread maximum that at least 15 per-thread maxima reach is at most the
+// 15th best (the 15 largest per-thread maxima are 15 distinct candidates), so the candidates
+// with key >= T contain the answer; they are ranked by counting, or, should more than 64
+// survive, warp 0 merges the whole range exactly by insertion. Ranges of up to 1,024
+// candidates are read once into registers (thread t: candidates lo + 8t .. lo + 8t + 7);
+// longer ones are streamed twice.
+__device__ __noinline__ void range_top15(const float* S, int lo, int hi, TopkScratch& tk, uint64_t* out) {
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  constexpr int L = kTopK - 1;
+  const bool direct = hi - lo <= 8 * 128;
+  uint64_t k8[8];
+  uint64_t mx = 0ull;
+  if (direct) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = lo + 8 * t + u;
+      v[u] = c < hi ? __ldcg(S + c) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int c = lo + 8 * t + u;
+      k8[u] = c < hi ? topk_key(v[u], c) : 0ull;
+      mx = k8[u] > mx ? k8[u] : mx;
+    }
+  } else {
+    for (int c0 = lo; c0 < hi; c0 += 4 * 128) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + t + 128 * u;
+        v[u] = c < hi ? __ldcg(S + c) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + t + 128 * u;
+        if (c < hi) {
+          const uint64_t k = topk_key(v[u], c);
+          mx = k > mx ? k : mx;
+        }
+      }
+    }
+  }
+  tk.lm[t] = mx;
+  if (t == 0) tk.cnt = 0;
+  named_bar_sync(2, 128);
+  int ge = 0;
+#pragma unroll 8
+  for (int j = 0; j < 128; ++j) ge += tk.lm[j] >= mx ? 1 : 0;
+  uint64_t T = (ge >= L && mx != 0ull) ? mx : 0ull;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const uint64_t o = shfl_xor_u64(T, off);
+    T = o > T ? o : T;
+  }
+  if (lane == 0) tk.tq[w] = T;
+  named_bar_sync(2, 128);
+  T = tk.tq[0];
+#pragma unroll
+  for (int q = 1; q < 4; ++q) T = tk.tq[q] > T ? tk.tq[q] : T;
+  auto keep_key = [&](uint64_t key, bool valid) {
+    const bool keep = valid && key >= T;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+    if (bal != 0u) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&tk.cnt, __popc(bal));
+      base = __shfl_sync(0xFFFFFFFFu, base, 0);
+      const int pos = base + __popc(bal & ((1u << lane) - 1u));
+      if (keep && pos < 64) tk.surv[pos] = key;
+    }
+  };
+  if (direct) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) keep_key(k8[u], k8[u] != 0ull);
+  } else {
+    for (int c0 = lo; c0 < hi; c0 += 4 * 128) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + t + 128 * u;
+        v[u] = c < hi ? __ldcg(S + c) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + t + 128 * u;
+        keep_key(topk_key(v[u], c), c < hi);
+      }
+    }
+  }
+  named_bar_sync(2, 128);
+  const int count = tk.cnt;
+  if (count <= 64) {
+    for (int i = t; i < count; i += 128) {
+      const uint64_t key = tk.surv[i];
+      int rank = 0;
+      for (int j = 0; j < count; ++j) rank += tk.surv[j] > key ? 1 : 0;
+      if (rank < L) out[rank] = key;
+    }
+    if (t >= count && t < L) out[t] = 0ull;
+  } else if (w == 0) {
+    // exact: per-lane sorted lists of 15 over the whole range, then a 15-round merge
+    uint64_t list[L];
+#pragma unroll
+    for (int j = 0; j < L; ++j) list[j] = 0ull;
+    for (int c = lo + lane; c < hi; c += 32) {
+      const uint64_t key = topk_key(__ldcg(S + c), c);
+      if (key > list[L - 1]) {
+#pragma unroll
+        for (int j = L - 1; j > 0; --j) list[j] = (key > list[j - 1]) ? list[j - 1] : ((key > list[j]) ? key : list[j]);
+        list[0] = key > list[0] ? key : list[0];
+      }
+    }
+#pragma unroll 1
+    for (int k = 0; k < L; ++k) {
+      uint64_t best = list[0];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = shfl_xor_u64(best, off);
+        best = o > best ? o : best;
+      }
+      if (best != 0ull && list[0] == best) {  // keys are unique per block id: exactly one lane
+#pragma unroll
+        for (int j = 0; j < L - 1; ++j) list[j] = list[j + 1];
+        list[L - 1] = 0ull;
+      }
+      if (lane == 0) out[k] = best;
+    }
+  }
+  named_bar_sync(2, 128);
+}
+
 }  // namespace
 
 // C = copies of the query rows down the 128-row tile (2: rows < 64; 4: rows < 32).
@@ -198,11 +342,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int r0 = p.q_indptr[b], R = p.q_indptr[b + 1] - r0;
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
                   r0 + R <= p.total_rows && kQPerKV * R <= p.max_m && kQPerKV * R <= kMpad;
-  if (!ok) {
-    if (tid == 0 && blockIdx.x == 0 && g == 0) set_flag(p.flags, kFlagBadLength);
+  if (!ok || R == 0) {
+    if (!ok && tid == 0 && blockIdx.x == 0 && g == 0) set_flag(p.flags, kFlagBadLength);
+    // nothing is selected for the group (when this kernel selects)
+    if (p.block_S != nullptr && blockIdx.x == 0 && tid < kTopK)
+      p.block_ids[(static_cast<long long>(b) * kGroups + g) * kTopK + tid] = -1;
     return;
   }
-  if (R == 0) return;
   const int nb = (N + kBlock - 1) / kBlock;
   const int M = kQPerKV * R;  // query rows of this (request, group): row m = speculative row m/8, head m%8
 
@@ -256,20 +402,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   __syncthreads();
 
-  pdl_wait_primary();  // the block ids come from the selection
+  pdl_wait_primary();  // the block ids (or the block scores) come from the selection
 
-  if (warp == 0) {
-    // the 16 ids in parallel; the valid ones keep their order (ballot ranks)
-    const int id = lane < kTopK ? p.block_ids[(static_cast<long long>(b) * kGroups + g) * kTopK + lane] : -1;
-    const bool valid = lane < kTopK && id >= 0 && id < nb;
-    if (lane < kTopK && !valid && id != -1 && blockIdx.x == 0) set_flag(p.flags, kFlagBadIds);
-    const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
-    if (valid) {
-      const int rank = __popc(vm & ((1u << lane) - 1u));
-      sm.ids[rank] = id;
-      sm.phys[rank] = bt_staged ? bt[id] : p.block_table[static_cast<long long>(b) * p.max_pages + id];
+  if (p.block_S == nullptr) {
+    if (warp == 0) {
+      // the 16 given ids in parallel; the valid ones keep their order (ballot ranks)
+      const int id = lane < kTopK ? p.block_ids[(static_cast<long long>(b) * kGroups + g) * kTopK + lane] : -1;
+      const bool valid = lane < kTopK && id >= 0 && id < nb;
+      if (lane < kTopK && !valid && id != -1 && blockIdx.x == 0) set_flag(p.flags, kFlagBadIds);
+      const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
+      if (valid) {
+        const int rank = __popc(vm & ((1u << lane) - 1u));
+        sm.ids[rank] = id;
+        sm.phys[rank] = bt_staged ? bt[id] : p.block_table[static_cast<long long>(b) * p.max_pages + id];
+      }
+      if (lane == 0) sm.nsel = __popc(vm);
     }
-    if (lane == 0) sm.nsel = __popc(vm);
+  } else {
+    // ---- the top-k of this group, fused [vLLM-zh "How MiniMax sparse attention works"; MSA-fig
+    // §1 TopK]: the recent block plus the 15 best others by block score (ties to the lower
+    // id); every block when there are at most 16. CTA s of the cluster ranks candidates
+    // [s nc / S, (s + 1) nc / S) to its 15 best, and each CTA merges the cluster's lists: the
+    // 15 best overall are among them, so the merge is exact. The split-0 CTA writes the ids.
+    const int S = p.splits;
+    const int rank = S > 1 ? static_cast<int>(cluster_rank()) : 0;
+    int32_t* ids_out = p.block_ids + (static_cast<long long>(b) * kGroups + g) * kTopK;
+    TopkScratch& tk = *reinterpret_cast<TopkScratch*>(sm.ktile[0]);
+    if (nb <= kTopK) {
+      if (warp == 0 && lane < kTopK) {
+        if (lane < nb) {
+          sm.ids[lane] = lane;
+          sm.phys[lane] = bt_staged ? bt[lane] : p.block_table[static_cast<long long>(b) * p.max_pages + lane];
+        }
+        if (rank == 0) ids_out[lane] = lane < nb ? lane : -1;
+        if (lane == 0) sm.nsel = nb;
+      }
+    } else {
+      const int nc = nb - 1;
+      const float* Sg = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
+      if (warp < 4) range_top15(Sg, rank * nc / S, (rank + 1) * nc / S, tk, sm.tk_local);
+      __syncthreads();
+      if (S > 1) cluster_sync_all();  // every CTA's list is in place
+      if (warp == 0) {
+        // gather the S lists (local or in the other CTAs' shared memory), then 15 rounds of
+        // taking the largest head
+        const uint32_t local_addr = smem_u32(sm.tk_local);
+        for (int i = lane; i < S * kTopK; i += 32) {
+          const int src = i / kTopK, k = i % kTopK;
+          tk.all[src][k] = k < kTopK - 1 ? (S > 1 ? ld_cluster_u64(cluster_map(local_addr + 8u * k, src))
+                                                  : sm.tk_local[k])
+                                         : 0ull;
+        }
+        __syncwarp();
+        int ptr = 0;
+        int32_t win = nb - 1;  // lane 15 keeps the recent block
+        for (int k = 0; k < kTopK - 1; ++k) {
+          uint64_t head = (lane < S && ptr < kTopK - 1) ? tk.all[lane][ptr] : 0ull;
+          uint64_t best = head;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const uint64_t o = shfl_xor_u64(best, off);
+            best = o > best ? o : best;
+          }
+          if (lane < S && head == best) ++ptr;  // keys are unique: one lane
+          if (lane == k) win = topk_id(best);
+        }
+        // the 16 ids ascending
+        int r = 0;
+#pragma unroll
+        for (int j = 0; j < kTopK; ++j) {
+          const int other = __shfl_sync(0xFFFFFFFFu, win, j);
+          r += other < win ? 1 : 0;
+        }
+        if (lane < kTopK) {
+          sm.ids[r] = win;
+          sm.phys[r] = bt_staged ? bt[win] : p.block_table[static_cast<long long>(b) * p.max_pages + win];
+          if (rank == 0) ids_out[r] = win;
+        }
+        if (lane == 0) sm.nsel = kTopK;
+      }
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();

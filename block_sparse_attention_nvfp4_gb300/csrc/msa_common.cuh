@@ -170,6 +170,11 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint64_t ld_cluster_u64(uint32_t caddr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(caddr) : "memory");
+  return v;
+}
 __device__ __forceinline__ float ld_cluster_f1(uint32_t caddr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");

@@ -47,7 +47,9 @@ struct AttnParams {
   const int32_t* context_lens;
   const int32_t* q_indptr;
   const int32_t* block_table;
-  const int32_t* block_ids;  // [B][4][16]
+  int32_t* block_ids;        // [B][4][16]: read, or written when block_S is set
+  const float* block_S;      // set: select the ids from these block scores in the kernel
+  int s_stride;              // row length of block_S ([B][4][s_stride])
   const uint8_t* q;
   const uint8_t* k_data;     // codes also read through tensor maps (launch_attn)
   const uint8_t* k_scale;
@@ -117,12 +119,13 @@ cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, lon
 // index-key operands are used). check_device: the current device is sm_103 (its SM
 // count returned). encode_code_map: the TMA view of an index-key code plane.
 // launch_selection: the scan (mode 0 fused, 1 per-token scores, 2 exact scores) and,
-// for modes 0 and 2, the chained top-k, with the given flags word and block-score
-// scratch ([B][4][score_stride(max_pages)] FP32).
+// for modes 0 and 2 with with_topk, the chained top-k, with the given flags word and
+// block-score scratch ([B][4][score_stride(max_pages)] FP32).
 msa_status validate(const msa_decode_args* a, bool need_kv, bool need_idx);
 msa_status check_device(int* sm_count);
 msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows);
 msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
-                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st);
+                            long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st,
+                            bool with_topk = true);
 
 }  // namespace msa

@@ -100,3 +100,40 @@ def kernel_form(nb, max_pages):
         return "direct"
     stride = (max_pages + 3) // 4 * 4
     return "staged" if 4 * stride * 4 <= 160 * 1024 else "warp"
+
+
+def attention_splits(num_reqs, sm_count):
+    """Splits per (request, group) of the attention (libmsa's launch plan): the fewest
+    blocks per split, a power of two in [2, 16], that fit every (request, group) x split
+    into one wave of sm_count CTAs."""
+    pairs = 4 * num_reqs
+    need = -(-16 * pairs // sm_count) if pairs else 16
+    bps = 1
+    while bps < need:
+        bps *= 2
+    bps = min(max(bps, 2), 16)
+    return 16 // bps
+
+
+def range_top15(block_scores, lo, hi):
+    """The attention kernel's top-k of candidates [lo, hi) for one CTA of a cluster: 128
+    threads; ranges of up to 1,024 candidates held 8 per thread (thread t: lo + 8t ..), longer
+    ones strided (thread t: lo + t + 128 i); T = the largest per-thread maximum that at least
+    15 per-thread maxima reach; more than 64 survivors take the exact insertion merge.
+    Returns (survivors, branch)."""
+    k = keys(block_scores[lo:hi], np.arange(lo, hi))
+    n = hi - lo
+    direct = n <= 1024
+    lm = np.zeros(128, np.uint64)
+    for t in range(128):
+        seg = k[8 * t:8 * t + 8] if direct else k[t::128]
+        lm[t] = seg.max() if len(seg) else 0
+    T = max((m for m in lm if m != 0 and np.sum(lm >= m) >= L), default=np.uint64(0))
+    n_surv = int(np.sum(k >= T))
+    return n_surv, ("insertion" if n_surv > 64 else "rank") + ("/direct" if direct else "/strided")
+
+
+def fused_branches(block_scores, nb, splits):
+    """range_top15's branch on every CTA of a (request, group) cluster of `splits` CTAs."""
+    nc = nb - 1
+    return [range_top15(block_scores, s * nc // splits, (s + 1) * nc // splits)[1] for s in range(splits)]

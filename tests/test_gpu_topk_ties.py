@@ -174,3 +174,43 @@ def test_signed_zero_scores_tie():
         want = oracle.select(blockv[g].astype(np.float64))
         assert np.array_equal(ids[0, g], want), (g, ids[0, g], want)
     assert np.array_equal(ids[0, 0], np.array(list(range(15)) + [nb - 1], np.int32))
+
+
+# msa_decode ranks requests of over 1,025 blocks inside its attention kernel when each
+# (request, group) is split over 4 or more CTAs: each CTA of the (request, group)'s cluster
+# ranks a share of the candidates and the cluster merges the shares' 15 best exactly.
+# (requests, pages, blocks, run, ranking branch one CTA must reach)
+FUSED = [
+    (1, 8, 3000, 8, "rank/direct"),            # 8 CTAs x ~375 candidates
+    (1, 4, 3000, 64, "insertion/direct"),      # long runs of one page in a CTA's share
+    (1, 8, 10000, 1, "rank/strided"),          # 8 CTAs x 1,250 candidates
+    (1, 128, 10000, 1, "insertion/strided"),   # each thread's share holds one page: 15 pages survive
+]
+
+
+def _aliased_batch(nreq, pages, nb, run, rows=1, seed=41):
+    one = aliased(pages, nb, run, rows=rows, seed=seed, tail=37)
+    wl = copy.copy(one)
+    wl.num_reqs = nreq
+    wl.context_lens = np.repeat(one.context_lens, nreq)
+    wl.block_table = np.repeat(one.block_table, nreq, axis=0)
+    wl.q_indptr = np.arange(nreq + 1, dtype=np.int32) * rows
+    wl.total_rows = nreq * rows
+    wl.q = np.tile(one.q, (nreq, 1, 1))
+    wl.q_idx = np.tile(one.q_idx, (nreq, 1, 1))
+    return wl
+
+
+@pytest.mark.gpu
+@gpu
+@pytest.mark.parametrize("nreq,pages,nb,run,branch", FUSED)
+def test_decode_with_the_topk_inside_the_attention(nreq, pages, nb, run, branch):
+    wl = _aliased_batch(nreq, pages, nb, run)
+    splits = _topk_sim.attention_splits(nreq, torch.cuda.get_device_properties(0).multi_processor_count)
+    dec = _gpu.decoder(wl, with_block_scores=True)
+    dec.select_blocks()                     # the same scan: the block scores the attention ranks
+    bs = dec.block_scores.cpu().numpy()
+    torch.cuda.synchronize()
+    got = {br for b in range(min(nreq, 2)) for g in range(4) for br in _topk_sim.fused_branches(bs[b, g], nb, splits)}
+    assert branch in got, (splits, got)
+    _gpu.check_decode(wl, dec=_gpu.decoder(wl))
