@@ -26,7 +26,7 @@ FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS, FLAG_BAD_SLOT = 0x1,
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
            "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact",
-           "msa_select_blocks_noalloc_get_error")
+           "msa_select_blocks_noalloc_get_error", "msa_dcp_local_topk", "msa_dcp_merge_topk")
 
 
 class MSAError(RuntimeError):
@@ -87,6 +87,9 @@ def load(path: str = LIB_PATH):
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_dequant_rows.argtypes = [vp, vp, i64, vp, ctypes.c_int32, vp]
             lib.msa_kv_insert_nvfp4.argtypes = [ctypes.POINTER(KvInsertArgs), vp, sz, vp]
+            i32 = ctypes.c_int32
+            lib.msa_dcp_local_topk.argtypes = [ap, i32, i32, vp, vp, sz, vp]
+            lib.msa_dcp_merge_topk.argtypes = [ap, i32, i32, i32, vp, vp, vp, sz, vp]
             for f in EXPORTS[1:]:
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -191,6 +194,20 @@ def msa_select_blocks_noalloc_get_error(stream=None) -> int:
     if code not in (MSA_OK, -5, -6):
         _check(code, "msa_select_blocks_noalloc_get_error")
     return int(flags.value)
+
+
+def msa_dcp_local_topk(args: Args, rank: int, world: int, cand_keys: torch.Tensor, ws: torch.Tensor, stream=None):
+    """cand_keys: int64 [4, B, 16] (the uint64 keys' bits)."""
+    _check(load().msa_dcp_local_topk(ctypes.byref(args), rank, world, _ptr(cand_keys), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)), "msa_dcp_local_topk")
+
+
+def msa_dcp_merge_topk(args: Args, world: int, group0: int, n_groups: int, all_keys: torch.Tensor,
+                       block_ids: torch.Tensor, ws: torch.Tensor, stream=None):
+    """all_keys: int64 [world, n_groups, B, 16]."""
+    _check(load().msa_dcp_merge_topk(ctypes.byref(args), world, group0, n_groups, _ptr(all_keys), _ptr(block_ids),
+                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "msa_dcp_merge_topk")
 
 
 def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],

@@ -205,7 +205,7 @@ WsLayout ws_layout(int num_reqs, int max_pages) {
 
 msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
                             long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st,
-                            bool with_topk) {
+                            bool with_topk, int shard, int nshards, uint64_t* dcp_keys) {
   // the scan's shared memory grows with the request count (its page prefix); the exact-score
   // layout leaves room for about 560 requests within the 227 KB a CTA may opt into
   if (select_smem_bytes(args->num_reqs, mode) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
@@ -225,6 +225,8 @@ msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids,
   p.ki_scale = args->ki_scale;
   p.block_S = block_S;
   p.s_stride = score_stride(args->max_pages_per_req);
+  p.shard = shard;
+  p.nshards = nshards;
   p.flags = flags;
   p.block_ids = ids;
   p.block_scores_out = scores_out;
@@ -232,6 +234,7 @@ msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids,
   p.score_stride = stride;
   if (launch_select(map, p, mode, sm_count, st) != cudaSuccess) return MSA_ERR_CUDA;
   if (mode != 1 && with_topk && launch_topk(p, st) != cudaSuccess) return MSA_ERR_CUDA;
+  if (dcp_keys != nullptr && launch_dcp_local(p, dcp_keys, st) != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }
 
@@ -317,6 +320,50 @@ msa_status msa_select_blocks_exact(const msa_decode_args* args, int32_t* block_i
   if (s != MSA_OK) return s;
   if (block_ids == nullptr) return MSA_ERR_INVALID_ARG;
   return run_select(args, 2, block_ids, block_scores, nullptr, 0, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_dcp_local_topk(const msa_decode_args* args, int32_t rank, int32_t world, uint64_t* cand_keys,
+                              void* ws, size_t ws_bytes, void* stream) {
+  msa_status s = validate(args, false, true);
+  if (s != MSA_OK) return s;
+  if (cand_keys == nullptr || (reinterpret_cast<uintptr_t>(cand_keys) & 7u) != 0 || world < 1 ||
+      world > MSA_DCP_MAX_WORLD || rank < 0 || rank >= world)
+    return MSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((s = check_device(&sms)) != MSA_OK) return s;
+  if (select_smem_bytes(args->num_reqs, 0) > 227 * 1024) return MSA_ERR_UNSUPPORTED;
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
+  return launch_selection(args, 0, nullptr, nullptr, nullptr, 0, w.flags, w.block_S, sms,
+                          static_cast<cudaStream_t>(stream), false, rank, world, cand_keys);
+}
+
+msa_status msa_dcp_merge_topk(const msa_decode_args* args, int32_t world, int32_t group0, int32_t n_groups,
+                              const uint64_t* all_keys, int32_t* block_ids, void* ws, size_t ws_bytes,
+                              void* stream) {
+  msa_status s = validate(args, false, false);
+  if (s != MSA_OK) return s;
+  if (all_keys == nullptr || block_ids == nullptr || (reinterpret_cast<uintptr_t>(all_keys) & 7u) != 0 ||
+      world < 1 || world > MSA_DCP_MAX_WORLD || group0 < 0 || n_groups < 1 || group0 + n_groups > kGroups)
+    return MSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((s = check_device(&sms)) != MSA_OK) return s;
+  Ws w;
+  if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
+  if (args->num_reqs == 0) return MSA_OK;
+  DcpMergeParams p = {};
+  p.num_reqs = args->num_reqs;
+  p.max_pages = args->max_pages_per_req;
+  p.total_rows = args->total_rows;
+  p.context_lens = args->context_lens;
+  p.q_indptr = args->q_indptr;
+  p.keys = all_keys;
+  p.world = world;
+  p.group0 = group0;
+  p.n_groups = n_groups;
+  p.block_ids = block_ids;
+  p.flags = w.flags;
+  return launch_dcp_merge(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scores, int64_t score_stride,

@@ -20,6 +20,8 @@ struct SelectParams {
   const uint8_t* ki_scale;
   float* block_S;           // workspace [B][4][s_stride] block scores
   int s_stride;             // max_pages rounded up to a multiple of 4 (16-byte rows)
+  int shard, nshards;       // scan logical blocks c with c % nshards == shard (0 of 1: all);
+                            // block_S column i holds block i * nshards + shard
   uint32_t* flags;          // workspace error flags
   int32_t* block_ids;       // [B][4][16]
   float* block_scores_out;  // optional [B][4][max_pages]
@@ -82,6 +84,18 @@ struct KvInsertParams {
   uint32_t* flags;
 };
 
+// Merge of the rank-local candidate lists of indexer decode context parallelism
+// (msa_dcp_merge_topk).
+struct DcpMergeParams {
+  int num_reqs, max_pages, total_rows;
+  const int32_t* context_lens;
+  const int32_t* q_indptr;
+  const uint64_t* keys;  // [world][n_groups][B][16] candidate keys
+  int world, group0, n_groups;
+  int32_t* block_ids;    // [B][4][16]: rows of groups group0 .. group0 + n_groups - 1 written
+  uint32_t* flags;
+};
+
 // Workspace layout, offsets in bytes (each 256-aligned).
 struct WsLayout {
   size_t flags, block_S, total;
@@ -106,6 +120,10 @@ cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, in
 // to the scan with programmatic dependent launch
 cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st);
 cudaError_t launch_maxpool_topk(const MaxpoolParams& prm, cudaStream_t st);
+// rank-local candidate lists [4][B][16] from a sharded scan's block scores (chained to the
+// scan), and their merge
+cudaError_t launch_dcp_local(const SelectParams& prm, uint64_t* keys, cudaStream_t st);
+cudaError_t launch_dcp_merge(const DcpMergeParams& prm, cudaStream_t st);
 // kmap / vmap: tensor maps of the K and V code planes (encode_code_map over num_pages * 4 * 128 rows)
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& prm, bool pdl,
                         cudaStream_t st);
@@ -120,12 +138,14 @@ cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, lon
 // count returned). encode_code_map: the TMA view of an index-key code plane.
 // launch_selection: the scan (mode 0 fused, 1 per-token scores, 2 exact scores) and,
 // for modes 0 and 2 with with_topk, the chained top-k, with the given flags word and
-// block-score scratch ([B][4][score_stride(max_pages)] FP32).
+// block-score scratch ([B][4][score_stride(max_pages)] FP32). With nshards > 1 the scan
+// covers the logical blocks c with c % nshards == shard (modes 0 and 2, no top-k) and, if
+// dcp_keys is set, the rank-local candidate lists follow it.
 msa_status validate(const msa_decode_args* a, bool need_kv, bool need_idx);
 msa_status check_device(int* sm_count);
 msa_status encode_code_map(CUtensorMap* map, const uint8_t* base, long long rows);
 msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids, float* scores_out, float* tok,
                             long long stride, uint32_t* flags, float* block_S, int sm_count, cudaStream_t st,
-                            bool with_topk = true);
+                            bool with_topk = true, int shard = 0, int nshards = 1, uint64_t* dcp_keys = nullptr);
 
 }  // namespace msa

@@ -118,6 +118,11 @@ static_assert(offsetof(SmemT<false>, codes) % 1024 == 0 && offsetof(SmemT<false>
 static_assert(offsetof(SmemT<false>, scales) % 16 == 0 && offsetof(SmemT<true>, scales) % 16 == 0,
               "bulk copies need 16-byte alignment");
 
+// A scan over one shard of every request's blocks (indexer decode context
+// parallelism): the shard's i-th block is logical block i * nshards + shard; a whole
+// scan is shard 0 of 1. Its block scores go to column i of block_S.
+__device__ __forceinline__ int shard_block(const SelectParams& p, int i) { return i * p.nshards + p.shard; }
+
 struct PageCursor {
   int b;       // request
   int c;       // logical block within the request
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       pages = 0;
     }
     if (R == 0) pages = 0;
-    prefix[b] = pages;
+    prefix[b] = pages > p.shard ? (pages - 1 - p.shard) / p.nshards + 1 : 0;  // this shard's blocks
   }
   __syncthreads();
   if (warp == 0) {  // exclusive prefix over requests: each lane scans a contiguous chunk
@@ -357,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (staged) {
     for (int i = tid; i < n; i += kThreads) {
       const PageCursor pc = cursor_at(p0 + i, prefix, B);
-      sm.phys[i] = p.block_table[static_cast<long long>(pc.b) * p.max_pages + pc.c];
+      sm.phys[i] = p.block_table[static_cast<long long>(pc.b) * p.max_pages + shard_block(p, pc.c)];
     }
   }
   // the first request's index queries
@@ -390,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           alive = wait_bar(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1, p.flags);
           if (!alive) break;
         }
-        const int phys = staged ? sm.phys[i] : p.block_table[static_cast<long long>(ld.b) * p.max_pages + ld.c];
+        const int phys =
+            staged ? sm.phys[i] : p.block_table[static_cast<long long>(ld.b) * p.max_pages + shard_block(p, ld.c)];
         const bool bad = phys < 0 || phys >= p.num_pages;
         const uint32_t bar = smem_u32(&sm.full[s]);
         if (bad) {
@@ -500,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (alive) alive = wait_bar(smem_u32(&sm.dfull[k]), (ip / kDBufs) & 1, p.flags);
       alive = __all_sync(0xFFFFFFFFu, alive) != 0;
       tc_fence_after();
-      const int b = pc.b, c = pc.c;
-      const int t0 = c * kBlock + 32 * quad;  // this quadrant's first token
+      const int b = pc.b, c = shard_block(p, pc.c);  // logical block of the request
+      const int t0 = c * kBlock + 32 * quad;         // this quadrant's first token
       const int lim = N - R + rq - t0;        // column u is visible to this row iff u <= lim
       const uint32_t d = d_lane + static_cast<uint32_t>(k) * kDCols;
       float m = -INFINITY;
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
         m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         if (lane < kGroups) sm.part[k][quad][lane] = m;
-        if (quad == 0 && lane == 0) sm.page_bc[k] = make_int2(b, c);
+        if (quad == 0 && lane == 0) sm.page_bc[k] = make_int2(b, pc.c);  // block_S column: the shard's index
         if ((it + 1) % kPoolBatch == 0 || ip + kPoolSets >= n) {
           named_bar_sync(1 + set, 128);
           const int pg = ip - kPoolSets * (it % kPoolBatch) + kPoolSets * (lane >> 2);
@@ -545,7 +551,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int kk = pg % kDBufs;
             const int2 bc = sm.page_bc[kk];
             // a page whose table entry is out of range scores -inf (its codes were never loaded)
-            const int phys = staged ? sm.phys[pg] : p.block_table[static_cast<long long>(bc.x) * p.max_pages + bc.y];
+            const int phys =
+                staged ? sm.phys[pg] : p.block_table[static_cast<long long>(bc.x) * p.max_pages + shard_block(p, bc.y)];
             const float mm = phys < 0 || phys >= p.num_pages
                                  ? -INFINITY
                                  : fmaxf(fmax3(sm.part[kk][0][g], sm.part[kk][1][g], sm.part[kk][2][g]),

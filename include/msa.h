@@ -85,7 +85,7 @@ typedef enum {
 #define MSA_FLAG_BAD_PAGE    0x1u   /* block_table entry outside [0, num_pages) */
 #define MSA_FLAG_BAD_LENGTH  0x2u   /* context_lens / q_indptr inconsistent with the limits */
 #define MSA_FLAG_TIMEOUT     0x4u   /* an mbarrier / async-copy wait hit its time limit */
-#define MSA_FLAG_BAD_IDS     0x8u   /* msa_sparse_attn_decode got a block id outside the context */
+#define MSA_FLAG_BAD_IDS     0x8u   /* msa_sparse_attn_decode got a block id outside the context, or msa_dcp_merge_topk a bad candidate list */
 #define MSA_FLAG_BAD_SLOT    0x10u  /* msa_kv_insert_nvfp4 got a slot on a page outside [0, num_pages) */
 
 typedef struct {
@@ -196,6 +196,53 @@ msa_status msa_select_blocks_noalloc(const msa_decode_args* args, int32_t* block
  * (MSA_ERR_TIMEOUT, MSA_ERR_BAD_TABLE), as msa_get_error does for a workspace. The
  * next msa_select_blocks_noalloc call clears them. Allocates nothing. */
 msa_status msa_select_blocks_noalloc_get_error(void* stream, uint32_t* flags);
+
+/* Indexer decode context parallelism (DCP) [vLLM-zh "NVFP4 indexer decode context
+ * parallelism"]: the context's pages are spread over `world` GPUs; each scores its
+ * share of every request for all four groups and sends its best blocks per group to
+ * the GPU(s) that need the selection, which merge the lists into the exact top-16
+ * (the same ids msa_select_blocks returns on one GPU, ties included). The two calls
+ * below run on either side of that exchange; the exchange itself (an NCCL
+ * all-gather of every rank's lists, or an all-to-all that sends group g's lists to
+ * the rank that owns group g) is the caller's.
+ *
+ * Partition: logical block c of every request belongs to rank c % world (the pages
+ * say only that each GPU scores its share of the context). A rank's args describe
+ * the whole batch (lengths, row pointers, the replicated index queries) with its own
+ * index-key cache: block_table entries are read only at the rank's own blocks and
+ * name pages of that rank's ki_data/ki_scale (num_pages = its page count). Entries at
+ * other ranks' blocks are never read.
+ *
+ * Candidate list: 16 uint64 keys per (group, request), best first: the rank's 15
+ * best blocks other than the request's most recent one (which the merge always keeps),
+ * zero-filled past the rank's count; slot 15 is always zero. A key is
+ *   (order image of the FP32 block score) << 32 | (0xFFFFFFFF - logical block id),
+ * where the order image of score bits u is u | 0x80000000 for a non-negative score
+ * (-0.0 counts as +0.0) and ~u for a negative one, so a larger key is a better block
+ * and equal scores rank the lower id first. 0 = no candidate. */
+#define MSA_DCP_MAX_WORLD 8
+
+/* The rank-local half: the index scan over rank `rank`'s blocks (0 <= rank < world
+ * <= MSA_DCP_MAX_WORLD), then its candidate lists. cand_keys (device, 8-byte aligned):
+ * [4][B][16] uint64, group-major so that group g's lists are one contiguous slice.
+ * Two kernels on `stream`, the second chained to the scan by programmatic dependent
+ * launch; uses the workspace's block-score scratch and flags as msa_select_blocks. */
+msa_status msa_dcp_local_topk(const msa_decode_args* args, int32_t rank, int32_t world, uint64_t* cand_keys,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* The merge: all_keys (device) [world][n_groups][B][16] holds, for groups group0 ..
+ * group0 + n_groups - 1, every rank's lists in rank order (an all-gather of
+ * cand_keys gives group0 = 0, n_groups = 4; an all-to-all of group slices gives one
+ * rank's own groups). Writes block_ids[B][4][16] rows of those groups (ascending,
+ * -1 padded, as msa_select_blocks); other groups' rows are left untouched. A key
+ * naming a block outside its rank's share, the recent block or a repeated block, or
+ * fewer than 15 candidates for a request of more than 16 blocks, sets
+ * MSA_FLAG_BAD_IDS in the workspace (msa_get_error: MSA_ERR_BAD_TABLE); such keys
+ * are dropped and missing winners leave -1 at the end of the row. Only the lengths
+ * and row pointers of args are read. */
+msa_status msa_dcp_merge_topk(const msa_decode_args* args, int32_t world, int32_t group0, int32_t n_groups,
+                              const uint64_t* all_keys, int32_t* block_ids, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, three
  * kernels on `stream`, each chained to the one before it with programmatic

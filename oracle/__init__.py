@@ -209,6 +209,41 @@ def select(S_g: np.ndarray, top_k: int = 16) -> np.ndarray:
     return ids
 
 
+# ---------------------------------------------------------------- indexer DCP
+# [vLLM-zh] "NVFP4 indexer decode context parallelism": the context is split over
+# the GPUs, each scores its part for all four heads (groups) and sends a local top
+# list per head; the owner merges the lists into the final top-16, and the result is
+# exact. Reading (the pages do not say how the context is split): logical block c
+# belongs to rank c % world. The recent block is kept by the merge, so a local list
+# holds the rank's top_k - 1 best other blocks.
+
+def dcp_blocks(nb: int, rank: int, world: int) -> list:
+    """Logical blocks of a request of nb blocks that rank `rank` of `world` scores."""
+    return [c for c in range(nb) if c % world == rank]
+
+
+def dcp_local_topk(S_g: np.ndarray, rank: int, world: int, top_k: int = 16) -> list:
+    """One group's local list on one rank: [(score, block id)] of the rank's blocks other
+    than the recent one, best first (higher score, then lower id), at most top_k - 1."""
+    nb = len(S_g)
+    cands = [(float(S_g[c]), c) for c in dcp_blocks(nb, rank, world) if c != nb - 1]
+    assert not any(np.isnan(s) for s, _ in cands)
+    cands.sort(key=lambda sc: (-sc[0], sc[1]))
+    return cands[:top_k - 1]
+
+
+def dcp_merge(lists, nb: int, top_k: int = 16) -> np.ndarray:
+    """The owner's merge of every rank's list for one group of a request of nb blocks:
+    the recent block plus the top_k - 1 best candidates of all lists; every block when
+    nb <= top_k. Ids ascending, -1 padded (the layout of select())."""
+    if nb <= top_k:
+        chosen = list(range(nb))
+    else:
+        pool = sorted((sc for lst in lists for sc in lst), key=lambda sc: (-sc[0], sc[1]))
+        chosen = sorted([c for _, c in pool[:top_k - 1]] + [nb - 1])
+    return np.array(chosen + [-1] * (top_k - len(chosen)), np.int32)
+
+
 def attend(wl, b: int, ids: np.ndarray):
     """Attention of request b over block ids [4, top_k]: (out [R,32,128], lse [R,32])."""
     N, R = _geom(wl, b)

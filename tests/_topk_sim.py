@@ -137,3 +137,17 @@ def fused_branches(block_scores, nb, splits):
     """range_top15's branch on every CTA of a (request, group) cluster of `splits` CTAs."""
     nc = nb - 1
     return [range_top15(block_scores, s * nc // splits, (s + 1) * nc // splits)[1] for s in range(splits)]
+
+
+def dcp_local(local_scores, nc):
+    """warp_best15 of the DCP rank-local lists: candidate i (the rank's i-th block,
+    recent block excluded) sits in lane i % 32; T = the 15th largest lane maximum.
+    Branches: "sort" (<= 32 survivors), "two_sorts" (33..64), "chunked" (> 64: the
+    candidates merged 32 at a time)."""
+    k = keys(local_scores[:nc])
+    lm = np.zeros(32, np.uint64)
+    for i in range(nc):
+        lm[i % 32] = max(lm[i % 32], k[i])
+    T = np.sort(lm)[::-1][L - 1]
+    n = int(np.sum((k >= T) & (k != 0)))
+    return n, ("chunked" if n > 64 else "two_sorts" if n > 32 else "sort")

@@ -96,3 +96,25 @@ def test_kv_insert_host_validation(lib):
     a = A(num_tokens=4, num_pages=1, slot_mapping=1 << 20, k=1 << 20, k_data=1 << 21, k_scale=1 << 22)
     assert f(ctypes.byref(a), None, 256, None) == -4     # no workspace
     assert f(ctypes.byref(a), ws, 16, None) == -4        # workspace too small
+
+
+def test_dcp_host_validation(lib):
+    """The DCP entry points reject bad ranks, worlds, group ranges and pointers before any
+    CUDA call."""
+    a = _args()
+    keys = ctypes.c_void_p(0x50000)
+    ws = ctypes.c_void_p(0x40000)
+    loc = lib.msa_dcp_local_topk
+    for rank, world in ((0, 0), (1, 1), (-1, 2), (2, 2), (0, 9)):
+        assert loc(ctypes.byref(a), rank, world, keys, ws, 1 << 20, None) == -1, (rank, world)
+    assert loc(ctypes.byref(a), 0, 2, None, ws, 1 << 20, None) == -1
+    assert loc(ctypes.byref(a), 0, 2, ctypes.c_void_p(0x50004), ws, 1 << 20, None) == -1  # not 8-byte aligned
+    assert loc(None, 0, 2, keys, ws, 1 << 20, None) == -1
+    mrg = lib.msa_dcp_merge_topk
+    ids = ctypes.c_void_p(0x60000)
+    for world, g0, ng in ((0, 0, 4), (9, 0, 4), (2, -1, 1), (2, 0, 0), (2, 3, 2), (2, 4, 1)):
+        assert mrg(ctypes.byref(a), world, g0, ng, keys, ids, ws, 1 << 20, None) == -1, (world, g0, ng)
+    assert mrg(ctypes.byref(a), 2, 0, 4, None, ids, ws, 1 << 20, None) == -1
+    assert mrg(ctypes.byref(a), 2, 0, 4, keys, None, ws, 1 << 20, None) == -1
+    a.head_dim = 64
+    assert mrg(ctypes.byref(a), 2, 0, 4, keys, ids, ws, 1 << 20, None) == -2
