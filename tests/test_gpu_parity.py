@@ -209,3 +209,24 @@ def test_host_io_step_matches_device_decode(ragged):
     io.outputs["out"].zero_()
     res = io.step()
     assert torch.equal(res["out"], out_ref) and torch.equal(res["lse"], lse_ref)
+
+
+@pytest.mark.parametrize("B", [1500, 2400])
+def test_many_requests(B):
+    """Thousands of short requests: the scan's page prefix (one entry per request) lives in
+    shared memory beside its buffers, and every CTA's pages span many requests. Block
+    scores equal the oracle's and the top-k is exact on the GPU's own scores."""
+    rng = np.random.default_rng(B)
+    ctx = [int(x) for x in rng.integers(1, 3000, B)]
+    wl = _wl.small(ctx, [1] * B, seed=41)
+    dec = _gpu.decoder(wl, with_block_scores=True)
+    ids = dec.select_blocks().cpu().numpy()
+    bs = dec.block_scores.cpu().numpy()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    for b in range(0, B, 7):
+        nb = (ctx[b] + 127) // 128
+        Sr = oracle.block_scores(wl, b)
+        np.testing.assert_allclose(bs[b, :, :nb], Sr, rtol=1e-5, atol=1e-4)
+        for g in range(4):
+            _gpu.assert_topk_exact_on_own_scores(ids[b, g], bs[b, g], nb, (b, g))
