@@ -253,6 +253,47 @@ def time_calls(fn, l2_flush, stream, reps):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def measure_dcp(l2_flush, stream, reps, name="long_512k", world=4):
+    """Indexer decode context parallelism emulated on one GPU: the rank-local half
+    (msa_dcp_local_topk: the scan of one rank's share of the blocks and its candidate
+    lists) for every rank of `world`, run one after another, and the merge of all ranks'
+    lists (msa_dcp_merge_topk, all-gather layout), against the single-GPU selection of
+    the same workload. Device times, L2 flushed before each call. The exchange between
+    GPUs (an NCCL all-gather of the lists) is not run: one GPU."""
+    import torch
+
+    from block_sparse_attention_nvfp4_gb300 import DecodeBatch, KVCache, MSADecoder, _lib
+    from block_sparse_attention_nvfp4_gb300 import synth
+
+    wl = synth.make_workload(synth.preset(name))
+    cache, batch = KVCache.from_host(wl), DecodeBatch.from_host(wl)
+    dec = MSADecoder(cache, batch, sm_scale=wl.sm_scale)
+    args = dec.args
+    B = wl.num_reqs
+    keys = [torch.zeros((4, B, 16), dtype=torch.int64, device="cuda") for _ in range(world)]
+    ids = torch.full((B, 4, 16), -1, dtype=torch.int32, device="cuda")
+    local_us = []
+    for r in range(world):
+        fn = (lambda rr: (lambda: _lib.msa_dcp_local_topk(args, rr, world, keys[rr], dec.ws)))(r)
+        for _ in range(3):
+            fn()
+        local_us.append(spread(time_calls(fn, l2_flush, stream, reps))["mean_us"])
+    all_keys = torch.stack(keys).contiguous()
+    merge = lambda: _lib.msa_dcp_merge_topk(args, world, 0, 4, all_keys, ids, dec.ws)  # noqa: E731
+    merge_us = spread(time_calls(merge, l2_flush, stream, reps))["mean_us"]
+    single_us = spread(time_calls(dec.select_blocks, l2_flush, stream, reps))["mean_us"]
+    torch.cuda.synchronize()
+    same = bool(torch.equal(ids, dec.block_ids))
+    flags = dec.errors()
+    out = {"workload": name, "world": world, "rank_local_us": [round(x, 2) for x in local_us],
+           "merge_us": round(merge_us, 2), "single_gpu_select_us": round(single_us, 2),
+           "exchange_bytes_per_rank": 4 * B * 16 * 8, "ids_equal_single_gpu": same, "device_error_flags": flags,
+           "what": "one GPU emulates the ranks one after another; the NCCL exchange is unmeasured (one GPU)"}
+    del dec, cache, batch, wl
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_preset(name, l2_flush, stream, reps, peak):
     """One workload shape's decode step, selection call and attention alone (device
     times, L2 flushed before each call, inputs resident), with its algorithmic bytes and
@@ -384,6 +425,10 @@ def run_libmsa(args, rank, world, dist):
             if name != args.workload:
                 presets[name] = measure_preset(name, l2_flush, stream, min(args.steps, 30), peak)
 
+    dcp = None
+    if not args.no_presets and world == 1:
+        dcp = measure_dcp(l2_flush, stream, min(args.steps, 30))
+
     # ---- end to end through the public API: a step from pinned host memory (HostIO: the
     # inputs packed into one buffer, one host-to-device copy, the decode, one
     # device-to-host copy of the packed outputs, synchronize), copies inside the timed region
@@ -450,6 +495,7 @@ def run_libmsa(args, rank, world, dist):
                                      "(FP16 tiles and MMAs), timed alone like the roofline call"},
             "kv_insert_nvfp4": kv_insert,
             "workloads": presets,
+            "dcp_emulated": dcp,
             "clocks": clocks, "timed_wall_s": round(wall, 4), "device_error_flags": ok_flags,
             "impl": "libmsa"}
     return line

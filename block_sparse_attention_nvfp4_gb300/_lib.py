@@ -26,7 +26,8 @@ FLAG_BAD_PAGE, FLAG_BAD_LENGTH, FLAG_TIMEOUT, FLAG_BAD_IDS, FLAG_BAD_SLOT = 0x1,
 EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa_get_error", "msa_index_scores",
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
            "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact",
-           "msa_select_blocks_noalloc_get_error", "msa_dcp_local_topk", "msa_dcp_merge_topk")
+           "msa_select_blocks_noalloc_get_error", "msa_dcp_local_topk", "msa_dcp_merge_topk",
+           "msa_selftest_wait_timeout")
 
 
 class MSAError(RuntimeError):
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH):
             i32 = ctypes.c_int32
             lib.msa_dcp_local_topk.argtypes = [ap, i32, i32, vp, vp, sz, vp]
             lib.msa_dcp_merge_topk.argtypes = [ap, i32, i32, i32, vp, vp, vp, sz, vp]
+            lib.msa_selftest_wait_timeout.argtypes = [vp, sz, vp]
             for f in EXPORTS[1:]:
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -208,6 +210,12 @@ def msa_dcp_merge_topk(args: Args, world: int, group0: int, n_groups: int, all_k
     _check(load().msa_dcp_merge_topk(ctypes.byref(args), world, group0, n_groups, _ptr(all_keys), _ptr(block_ids),
                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "msa_dcp_merge_topk")
+
+
+def msa_selftest_wait_timeout(ws: torch.Tensor, stream=None):
+    """Launch the bounded-wait diagnostic (include/msa.h); read the outcome with msa_get_error."""
+    _check(load().msa_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "msa_selftest_wait_timeout")
 
 
 def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor],

@@ -240,9 +240,35 @@ msa_status launch_selection(const msa_decode_args* args, int mode, int32_t* ids,
 
 }  // namespace msa
 
+namespace msa {
+namespace {
+
+// One thread waits, through the library's bounded wait, on phase 0 of an mbarrier that
+// nothing arrives at: the wait gives up after its limit, sets the timeout flag and returns.
+__global__ void selftest_timeout_kernel(uint32_t* flags) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  mbar_fence_init();
+  mbar_wait(smem_u32(&bar), 0, flags);
+}
+
+}  // namespace
+}  // namespace msa
+
 using namespace msa;
 
 extern "C" {
+
+msa_status msa_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & (kWsAlign - 1)) != 0 || ws_bytes < 256)
+    return MSA_ERR_WORKSPACE;
+  int sms = 0;
+  msa_status s = check_device(&sms);
+  if (s != MSA_OK) return s;
+  selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(ws));
+  return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
 
 const char* msa_status_string(msa_status s) {
   switch (s) {

@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kCand = kTopK - 1;  // 15 candidates per list
 constexpr int kSlots = kTopK;     // list row: 16 keys = 128 bytes
-constexpr int kDcpThreads = 32 * kGroups;
+constexpr int kDcpThreads = 32 * 4 * kGroups;  // four warps per group
 
 // Descending order of a bitonic sequence held one value per lane (half-cleaners only).
 __device__ __forceinline__ uint64_t warp_bitonic_merge_desc(uint64_t v) {
@@ -49,48 +49,68 @@ __device__ __forceinline__ uint64_t top32_union(uint64_t a, uint64_t b) {
   return warp_bitonic_merge_desc(a > r ? a : r);
 }
 
-// Keys of candidates 0 .. nc-1 of S (block scores an earlier kernel wrote: loads bypass
-// L1), id field = candidate index; batch `base` gives lane l the candidates base + 32u + l.
-__device__ __forceinline__ void load_keys8(const float* S, int nc, int base, uint64_t (&k)[8]) {
+// Keys of candidates c0 .. c1-1 of S (block scores an earlier kernel wrote: loads bypass
+// L1), id field = candidate index; batch `base` gives lane l the candidates
+// c0 + base + 32u + l, u < 8. All 8 loads are issued before the keys are formed.
+__device__ __forceinline__ void load_keys8(const float* S, int c0, int c1, int base, uint64_t (&k)[8]) {
   const int lane = threadIdx.x & 31;
   float v[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int c = base + 32 * u + lane;
-    v[u] = c < nc ? __ldcg(S + c) : 0.f;
+    const int c = c0 + base + 32 * u + lane;
+    v[u] = c < c1 ? __ldcg(S + c) : 0.f;
   }
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int c = base + 32 * u + lane;
-    k[u] = c < nc ? topk_key(v[u], c) : 0ull;
+    const int c = c0 + base + 32 * u + lane;
+    k[u] = c < c1 ? topk_key(v[u], c) : 0ull;
   }
 }
 
-// The 15 largest keys of candidates 0 .. nc-1, descending: lane i < 15 returns the i-th
+// Gather the keys >= T of one batch into surv (up to 64), counting all of them.
+__device__ __forceinline__ void keep_survivors(const uint64_t (&k)[8], uint64_t T, uint64_t* surv, int& count) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const bool keep = k[u] != 0ull && k[u] >= T;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+    const int pos = count + __popc(bal & ((1u << lane) - 1u));
+    if (keep && pos < 64) surv[pos] = k[u];
+    count += __popc(bal);
+  }
+}
+
+// The 15 largest keys of candidates c0 .. c1-1, descending: lane i < 15 returns the i-th
 // (0 past the end). The 15th largest lane maximum T is at most the 15th largest key, so
 // the keys >= T hold the answer; they are gathered (up to 64) and sorted. If more than 64
-// pass, the candidates are merged 32 at a time into a running top 32 instead.
-__device__ uint64_t warp_best15(const float* S, int nc, uint64_t* surv) {
+// pass, the candidates are merged 32 at a time into a running top 32 instead. Ranges of
+// at most 256 candidates are read once, into registers; longer ones are streamed twice.
+__device__ uint64_t warp_best15(const float* S, int c0, int c1, uint64_t* surv) {
   const int lane = threadIdx.x & 31;
+  const int n = c1 - c0;
   uint64_t lmax = 0ull;
-  for (int base = 0; base < nc; base += 256) {
-    uint64_t k[8];
-    load_keys8(S, nc, base, k);
+  uint64_t kr[8];
+  if (n <= 256) {
+    load_keys8(S, c0, c1, 0, kr);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) lmax = k[u] > lmax ? k[u] : lmax;
+    for (int u = 0; u < 8; ++u) lmax = kr[u] > lmax ? kr[u] : lmax;
+  } else {
+    for (int base = 0; base < n; base += 256) {
+      uint64_t k[8];
+      load_keys8(S, c0, c1, base, k);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lmax = k[u] > lmax ? k[u] : lmax;
+    }
   }
   const uint64_t T = shfl_u64(warp_sort_desc(lmax), kCand - 1);
   int count = 0;
-  for (int base = 0; base < nc; base += 256) {
-    uint64_t k[8];
-    load_keys8(S, nc, base, k);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool keep = k[u] != 0ull && k[u] >= T;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-      const int pos = count + __popc(bal & ((1u << lane) - 1u));
-      if (keep && pos < 64) surv[pos] = k[u];
-      count += __popc(bal);
+  if (n <= 256) {
+    keep_survivors(kr, T, surv, count);
+  } else {
+    for (int base = 0; base < n; base += 256) {
+      uint64_t k[8];
+      load_keys8(S, c0, c1, base, k);
+      keep_survivors(k, T, surv, count);
     }
   }
   __syncwarp();
@@ -103,9 +123,14 @@ __device__ uint64_t warp_best15(const float* S, int nc, uint64_t* surv) {
     top = top32_union(a, b);
   } else {
     top = 0ull;
-    for (int base = 0; base < nc; base += 256) {
+    for (int base = 0; base < n; base += 256) {
       uint64_t k[8];
-      load_keys8(S, nc, base, k);
+      if (n <= 256) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) k[u] = kr[u];
+      } else {
+        load_keys8(S, c0, c1, base, k);
+      }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const uint64_t kk = k[u] >= T ? k[u] : 0ull;
@@ -118,11 +143,15 @@ __device__ uint64_t warp_best15(const float* S, int nc, uint64_t* surv) {
 }
 
 // Rank-local lists, after the scan of the rank's blocks (chained to it by programmatic
-// dependent launch): one CTA per request, warp g for group g. block_S column i holds
-// the score of logical block i * world + rank.
+// dependent launch): one CTA per request, four warps per group, warp q of group g taking
+// a quarter of the group's candidates; the group's warp 0 merges the four quarter lists
+// (each the exact best 15 of its quarter, so their union holds the group's best 15).
+// block_S column i holds the score of logical block i * world + rank.
 __global__ void __launch_bounds__(kDcpThreads) dcp_local_kernel(const SelectParams p, uint64_t* keys) {
-  __shared__ uint64_t surv[kGroups][64];
-  const int b = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ uint64_t surv[kGroups][4][64];
+  __shared__ uint64_t lists[kGroups][4][kSlots];
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = warp >> 2, q = warp & 3;
   const int N = p.context_lens[b];
   const int r0 = p.q_indptr[b], R = p.q_indptr[b + 1] - r0;
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
@@ -132,8 +161,16 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_local_kernel(const SelectPara
   // the recent block (nb - 1) is kept by the merge and is no candidate
   const int nc = nb > 0 && (nb - 1) % p.nshards == p.shard ? nloc - 1 : nloc;
   pdl_wait_primary();  // the block scores come from the scan
+  const int c0 = q * nc / 4, c1 = (q + 1) * nc / 4;
   uint64_t k = 0ull;
-  if (nc > 0) k = warp_best15(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride, nc, surv[g]);
+  if (c1 > c0) k = warp_best15(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride, c0, c1, surv[g][q]);
+  if (lane < kSlots) lists[g][q][lane] = k;
+  named_bar_sync(1 + g, 128);
+  if (q != 0) return;
+  uint64_t top = lane < kSlots ? lists[g][0][lane] : 0ull;
+#pragma unroll
+  for (int w = 1; w < 4; ++w) top = top32_union(top, lane < kSlots ? lists[g][w][lane] : 0ull);
+  k = lane < kCand ? top : 0ull;
   if (k != 0ull) {  // candidate index i -> logical block i * world + rank
     const uint32_t id = static_cast<uint32_t>(topk_id(k) * p.nshards + p.shard);
     k = (k & 0xFFFFFFFF00000000ull) | static_cast<uint64_t>(0xFFFFFFFFu - id);
@@ -146,7 +183,7 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_local_kernel(const SelectPara
 // rank other than the recent one, keeps the 15 best and adds the recent block; ids
 // ascending, as the single-GPU selection writes them. A list that breaks those rules
 // (a corrupt or truncated exchange) sets MSA_FLAG_BAD_IDS; its bad keys are dropped.
-__global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpMergeParams p) {
+__global__ void __launch_bounds__(32 * kGroups) dcp_merge_kernel(const DcpMergeParams p) {
   const int b = blockIdx.x, gl = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (gl >= p.n_groups) return;
   const int g = p.group0 + gl;
@@ -161,13 +198,20 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_merge_kernel(const DcpMergePa
     if (lane < kTopK) ids[lane] = lane < nb ? lane : -1;
     return;
   }
-  const int n = p.world * kSlots;
+  const int n = p.world * kSlots;  // at most 4 keys per lane (world <= 8)
+  uint64_t kin[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int i = 32 * t + lane, w = i / kSlots, j = i % kSlots;
+    kin[t] = i < n ? __ldcg(p.keys + ((static_cast<long long>(w) * p.n_groups + gl) * p.num_reqs + b) * kSlots + j)
+                   : 0ull;
+  }
   bool bad = false;
   uint64_t top = 0ull;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane, w = i / kSlots, j = i % kSlots;
-    uint64_t k = i < n ? __ldcg(p.keys + ((static_cast<long long>(w) * p.n_groups + gl) * p.num_reqs + b) * kSlots + j)
-                       : 0ull;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int i = 32 * t + lane, w = i / kSlots;
+    uint64_t k = kin[t];
     if (k != 0ull) {
       const int id = topk_id(k);
       if (id < 0 || id >= nb - 1 || id % p.world != w) {
@@ -218,7 +262,7 @@ cudaError_t launch_dcp_local(const SelectParams& prm, uint64_t* keys, cudaStream
 }
 
 cudaError_t launch_dcp_merge(const DcpMergeParams& prm, cudaStream_t st) {
-  dcp_merge_kernel<<<prm.num_reqs, kDcpThreads, 0, st>>>(prm);
+  dcp_merge_kernel<<<prm.num_reqs, 32 * kGroups, 0, st>>>(prm);
   return cudaGetLastError();
 }
 

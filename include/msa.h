@@ -124,6 +124,14 @@ msa_status msa_workspace_size(const msa_decode_args* args, size_t* bytes);
 /* Zero-fill a workspace (async memset on `stream`). Needed once per workspace. */
 msa_status msa_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
+/* Diagnostic for the failure path: one thread on the device waits, through the same
+ * bounded wait every kernel of the library uses, on a barrier phase that never
+ * completes. After the wait limit (1 s of %globaltimer) it sets MSA_FLAG_TIMEOUT in
+ * `ws` (at least 256 bytes, 256-byte aligned) and returns; the GPU context stays
+ * usable and msa_get_error then returns MSA_ERR_TIMEOUT. Nothing else is launched,
+ * no copy is in flight and no tensor memory is held while it waits. */
+msa_status msa_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* Read and clear the device error flags in `ws` (synchronises `stream`).
  * *flags (host) receives MSA_FLAG_* bits; returns MSA_OK when none is set,
  * else the matching error code. */

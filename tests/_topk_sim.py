@@ -140,14 +140,22 @@ def fused_branches(block_scores, nb, splits):
 
 
 def dcp_local(local_scores, nc):
-    """warp_best15 of the DCP rank-local lists: candidate i (the rank's i-th block,
-    recent block excluded) sits in lane i % 32; T = the 15th largest lane maximum.
-    Branches: "sort" (<= 32 survivors), "two_sorts" (33..64), "chunked" (> 64: the
-    candidates merged 32 at a time)."""
+    """warp_best15 of the DCP rank-local lists: four warps per group, warp q taking the
+    candidates [q nc / 4, (q + 1) nc / 4) (the rank's blocks in order, recent block
+    excluded), candidate c0 + i in lane i % 32; T = the 15th largest lane maximum of the
+    warp. Returns the branch of each warp: "sort" (<= 32 survivors), "two_sorts" (33..64),
+    "chunked" (> 64: the candidates merged 32 at a time)."""
     k = keys(local_scores[:nc])
-    lm = np.zeros(32, np.uint64)
-    for i in range(nc):
-        lm[i % 32] = max(lm[i % 32], k[i])
-    T = np.sort(lm)[::-1][L - 1]
-    n = int(np.sum((k >= T) & (k != 0)))
-    return n, ("chunked" if n > 64 else "two_sorts" if n > 32 else "sort")
+    out = []
+    for q in range(4):
+        c0, c1 = q * nc // 4, (q + 1) * nc // 4
+        if c1 <= c0:
+            continue
+        kq = k[c0:c1]
+        lm = np.zeros(32, np.uint64)
+        for i in range(len(kq)):
+            lm[i % 32] = max(lm[i % 32], kq[i])
+        T = np.sort(lm)[::-1][L - 1]
+        n = int(np.sum((kq >= T) & (kq != 0)))
+        out.append((n, "chunked" if n > 64 else "two_sorts" if n > 32 else "sort"))
+    return out

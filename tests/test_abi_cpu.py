@@ -118,3 +118,9 @@ def test_dcp_host_validation(lib):
     assert mrg(ctypes.byref(a), 2, 0, 4, keys, None, ws, 1 << 20, None) == -1
     a.head_dim = 64
     assert mrg(ctypes.byref(a), 2, 0, 4, keys, ids, ws, 1 << 20, None) == -2
+
+
+def test_selftest_host_validation(lib):
+    assert lib.msa_selftest_wait_timeout(None, 256, None) == -4
+    assert lib.msa_selftest_wait_timeout(ctypes.c_void_p(0x40010), 256, None) == -4  # misaligned
+    assert lib.msa_selftest_wait_timeout(ctypes.c_void_p(0x40000), 16, None) == -4   # too small

@@ -118,7 +118,7 @@ def check_lists(ranks, bs):
                 assert [float(x) for x in s[g, b, :n]] == [v for v, _ in want], (r, b, g)
                 loc = [c for c in range(r, nb, world) if c != nb - 1]
                 if loc:
-                    branches.add(_topk_sim.dcp_local(bs[b, g, loc], len(loc))[1])
+                    branches.update(br for _, br in _topk_sim.dcp_local(bs[b, g, loc], len(loc)))
     return branches
 
 
@@ -149,11 +149,12 @@ def test_dcp_equals_single_gpu_selection(name, world):
 # tie-heavy single requests (logical blocks aliased onto a few pages): each reaches the
 # named filter branch of the rank-local list on at least one (rank, group)
 TIES = [
-    (8, 300, 1, 1, "chunked"),
-    (8, 300, 1, 2, "two_sorts"),
+    (8, 3000, 8, 1, "chunked"),     # quarters of ~750 candidates: streamed, > 64 survivors
+    (8, 5000, 16, 2, "chunked"),    # quarters of ~625: streamed
+    (8, 3000, 8, 4, "chunked"),     # quarters of ~187: held in registers, > 64 survivors
+    (4, 3000, 8, 4, "two_sorts"),   # registers, 33..64 survivors
+    (8, 1100, 1, 2, "two_sorts"),
     (8, 300, 1, 4, "sort"),
-    (8, 3000, 8, 4, "chunked"),
-    (4, 1100, 64, 8, "two_sorts"),
 ]
 
 

@@ -111,3 +111,24 @@ def test_attention_block_ids_outside_the_context():
         else:
             ro = ref["out"][r0:r1]
         _gpu.assert_out_close(out[r0:r1], ro, f"request {b}")
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable():
+    """The library's bounded wait, run on a barrier phase that never completes
+    (msa_selftest_wait_timeout), gives up after its limit and reports MSA_FLAG_TIMEOUT
+    through the workspace; the next decode on the same context is correct."""
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    t0 = time.perf_counter()
+    _lib.msa_selftest_wait_timeout(ws)
+    flags = _lib.msa_get_error(ws)
+    dt = time.perf_counter() - t0
+    assert flags == _lib.FLAG_TIMEOUT
+    assert 0.9 < dt < 30.0, dt  # the limit is 1 s of the device timer
+    assert _lib.msa_get_error(ws) == 0  # read and cleared
+    wl = _base()
+    dec = _gpu.decoder(wl)
+    dec.decode()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    _check_others(wl, dec, [])
