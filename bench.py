@@ -501,6 +501,20 @@ def run_libmsa(args, rank, world, dist):
     return line
 
 
+def run_dcp_only(args):
+    """The emulated indexer-DCP timings alone (measure_dcp) for --workload at --dcp ranks."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    sink = torch.empty(1, dtype=torch.int64, device="cuda")
+
+    def l2_flush():
+        flush.zero_()
+        torch.sum(flush.view(torch.int64), dim=0, keepdim=True, out=sink)
+
+    return measure_dcp(l2_flush, torch.cuda.current_stream(), max(args.steps, 1), name=args.workload,
+                       world=args.dcp)
+
+
 # ----------------------------------------------------------------------------- reference arm (oracle)
 def run_reference(args):
     """The oracle as it stands, on the host cores (OpenMP over requests), on the same
@@ -558,6 +572,8 @@ def main():
     ap.add_argument("--workload", default="spec8_128k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-presets", action="store_true", help="skip the other workload shapes' figures")
+    ap.add_argument("--dcp", type=int, default=0, metavar="WORLD",
+                    help="only the emulated indexer-DCP timings of --workload at WORLD ranks (one JSON line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -579,6 +595,10 @@ def main():
         raise SystemExit("--gpus N>1 runs under torchrun (one process per GPU)")
     import __graft_entry__
     __graft_entry__.build()
+    if args.dcp:
+        if rank == 0:
+            print(json.dumps(run_dcp_only(args)), flush=True)
+        return
     line = run_libmsa(args, rank, world, dist)
     if rank == 0:
         print(json.dumps(line), flush=True)
