@@ -316,10 +316,15 @@ def measure_preset(name, l2_flush, stream, reps, peak):
     smsa = time_calls(dec.select_blocks, l2_flush, stream, reps)
     amsa = time_calls(lambda: dec.sparse_attn(ids), l2_flush, stream, reps)
     rows = np.diff(wl.q_indptr)
+    # groups of at most 16 query rows: the warp-MMA form of the attention, for comparison
+    small = None
+    if int(rows.max(initial=0)) <= 2:
+        small = spread(time_calls(lambda: dec.sparse_attn_small_rows(ids), l2_flush, stream, reps))["mean_us"]
     sb = bm.step_bytes(wl.context_lens, rows, ids.cpu().numpy())
     d = spread(dmsa)
     step_s = d["mean_us"] * 1e-6
     out = {"decode": d, "select_us": spread(smsa)["mean_us"], "attention_us": spread(amsa)["mean_us"],
+           "attention_small_rows_us": small,
            "query_rows": int(rows.sum()), "query_rows_per_s": round(float(rows.sum()) / step_s, 1),
            "step_bytes": sb["total"], "achieved_gbs": round(sb["total"] / step_s / 1e9, 1),
            "frac": round(sb["total"] / step_s / 1e9 / peak, 4), "reps": reps, "device_error_flags": flags}

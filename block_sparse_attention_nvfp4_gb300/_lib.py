@@ -27,7 +27,7 @@ EXPORTS = ("msa_status_string", "msa_workspace_size", "msa_workspace_init", "msa
            "msa_block_maxpool_topk", "msa_select_blocks", "msa_select_blocks_noalloc", "msa_sparse_attn_decode",
            "msa_decode", "msa_dequant_rows", "msa_kv_insert_nvfp4", "msa_select_blocks_exact",
            "msa_select_blocks_noalloc_get_error", "msa_dcp_local_topk", "msa_dcp_merge_topk",
-           "msa_selftest_wait_timeout")
+           "msa_selftest_wait_timeout", "msa_sparse_attn_decode_small_rows")
 
 
 class MSAError(RuntimeError):
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH):
             lib.msa_select_blocks_noalloc.argtypes = [ap, vp, vp, vp]
             lib.msa_select_blocks_noalloc_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.msa_sparse_attn_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
+            lib.msa_sparse_attn_decode_small_rows.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_decode.argtypes = [ap, vp, vp, vp, vp, sz, vp]
             lib.msa_dequant_rows.argtypes = [vp, vp, i64, vp, ctypes.c_int32, vp]
             lib.msa_kv_insert_nvfp4.argtypes = [ctypes.POINTER(KvInsertArgs), vp, sz, vp]
@@ -222,6 +223,13 @@ def msa_sparse_attn_decode(args: Args, block_ids: torch.Tensor, out: torch.Tenso
                            ws: torch.Tensor, stream=None):
     _check(load().msa_sparse_attn_decode(ctypes.byref(args), _ptr(block_ids), _ptr(out), _ptr(lse), _ptr(ws),
                                          ws.numel() * ws.element_size(), _stream(stream)), "msa_sparse_attn_decode")
+
+
+def msa_sparse_attn_decode_small_rows(args: Args, block_ids: torch.Tensor, out: torch.Tensor,
+                                      lse: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    _check(load().msa_sparse_attn_decode_small_rows(ctypes.byref(args), _ptr(block_ids), _ptr(out), _ptr(lse),
+                                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "msa_sparse_attn_decode_small_rows")
 
 
 def msa_decode_ptrs(args: Args, ids_p, out_p, lse_p, ws_p, ws_bytes: int, stream=None):

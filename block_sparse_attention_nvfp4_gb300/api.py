@@ -119,6 +119,13 @@ class MSADecoder:
         _lib.msa_sparse_attn_decode(self.args, block_ids, self.out.view(torch.int16), self.lse, self.ws, stream)
         return self.out
 
+    def sparse_attn_small_rows(self, block_ids: torch.Tensor, stream=None):
+        """The attention with warp-level MMAs (msa_sparse_attn_decode_small_rows; at most 2
+        rows per request)."""
+        _lib.msa_sparse_attn_decode_small_rows(self.args, block_ids, self.out.view(torch.int16), self.lse, self.ws,
+                                               stream)
+        return self.out
+
     def index_scores(self, stream=None) -> torch.Tensor:
         stride = self.batch.block_table.shape[1] * 128
         s = torch.full((self.batch.total_rows, 4, stride), float("nan"), dtype=torch.float32,

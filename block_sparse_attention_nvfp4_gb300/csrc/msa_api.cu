@@ -423,7 +423,7 @@ msa_status msa_block_maxpool_topk(const msa_decode_args* args, const float* scor
 // fused: the attention kernel selects the ids itself from the block scores the scan left in
 // the workspace (and writes them to ids); otherwise it reads the given ids
 static msa_status run_attn(const msa_decode_args* args, int32_t* ids, uint16_t* out, float* lse, void* ws,
-                           size_t ws_bytes, cudaStream_t st, bool pdl, bool fused) {
+                           size_t ws_bytes, cudaStream_t st, bool pdl, bool fused, bool small_rows = false) {
   int sms = 0;
   msa_status s = check_device(&sms);
   if (s != MSA_OK) return s;
@@ -441,6 +441,7 @@ static msa_status run_attn(const msa_decode_args* args, int32_t* ids, uint16_t* 
     p.block_S = w.block_S;
     p.s_stride = score_stride(args->max_pages_per_req);
   }
+  if (small_rows) return launch_attn_small(kmap, vmap, p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
   return launch_attn(kmap, vmap, p, pdl, st) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
@@ -451,6 +452,17 @@ msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* bl
   if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
   return run_attn(args, const_cast<int32_t*>(block_ids), out_bf16, lse, ws, ws_bytes,
                   static_cast<cudaStream_t>(stream), false, false);
+}
+
+msa_status msa_sparse_attn_decode_small_rows(const msa_decode_args* args, const int32_t* block_ids,
+                                             uint16_t* out_bf16, float* lse, void* ws, size_t ws_bytes,
+                                             void* stream) {
+  msa_status s = validate(args, true, false);
+  if (s != MSA_OK) return s;
+  if (block_ids == nullptr || out_bf16 == nullptr) return MSA_ERR_INVALID_ARG;
+  if (kQPerKV * args->max_rows_per_req > 16) return MSA_ERR_UNSUPPORTED;
+  return run_attn(args, const_cast<int32_t*>(block_ids), out_bf16, lse, ws, ws_bytes,
+                  static_cast<cudaStream_t>(stream), false, false, true);
 }
 
 msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse, void* ws,

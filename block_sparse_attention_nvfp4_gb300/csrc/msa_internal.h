@@ -127,6 +127,11 @@ cudaError_t launch_dcp_merge(const DcpMergeParams& prm, cudaStream_t st);
 // kmap / vmap: tensor maps of the K and V code planes (encode_code_map over num_pages * 4 * 128 rows)
 cudaError_t launch_attn(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& prm, bool pdl,
                         cudaStream_t st);
+// the same step for (request, group) pairs of at most 16 query rows (R <= 2): warp-level MMAs,
+// one CTA per pair; reads block_ids (never selects: block_S must be null)
+size_t attn_small_smem_bytes();
+cudaError_t launch_attn_small(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& prm, bool pdl,
+                              cudaStream_t st);
 cudaError_t launch_kv_insert(const KvInsertParams& prm, int sm_count, cudaStream_t st);
 cudaError_t launch_dequant_rows(const uint8_t* codes, const uint8_t* scales, long long nrows, uint8_t* out, int path,
                                 cudaStream_t st);

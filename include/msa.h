@@ -178,6 +178,22 @@ msa_status msa_select_blocks_exact(const msa_decode_args* args, int32_t* block_i
 msa_status msa_sparse_attn_decode(const msa_decode_args* args, const int32_t* block_ids,
                                   uint16_t* out_bf16, float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/* msa_sparse_attn_decode for batches whose (request, group) pairs have at most 16 query
+ * rows (max_rows_per_req <= 2, else MSA_ERR_UNSUPPORTED), with warp-level MMAs instead of
+ * the 128-row tensor-core tile: S = Q K^T by mma.sync m16n8k32 (E4M3 x E4M3, FP32
+ * accumulation), an online softmax in FP32 per warp over 16 keys of every block, P (FP16)
+ * times V (FP16, exact E4M3 values) by mma.sync m16n8k16, the 8 warps' partials merged
+ * with the log-sum-exp rule. One CTA per (request, group). Same arguments, outputs, flags
+ * and workspace as msa_sparse_attn_decode (a block on a page outside the cache is left out
+ * and flagged). The alternative for rows that fill only a small part of a tensor-core tile
+ * [vLLM-zh, Blackwell MSA kernels: tensor-core MMA once the query rows fill a tile]; on
+ * GB300 it measured slower than msa_sparse_attn_decode (32.8-34.5 vs 28.7 us for 32
+ * requests x 65,536 tokens x 1 row; 30.7-32.6 vs 16.1 us for 1 x 4,096 x 1), which
+ * therefore serves every row count in msa_decode. */
+msa_status msa_sparse_attn_decode_small_rows(const msa_decode_args* args, const int32_t* block_ids,
+                                             uint16_t* out_bf16, float* lse, void* ws, size_t ws_bytes,
+                                             void* stream);
+
 /* msa_select_blocks for callers that cannot allocate device memory. The MSA
  * pages have no counterpart to this entry point; it exists for hosts that hand a
  * library only the tensors it works on and keep the allocator to themselves

@@ -242,3 +242,44 @@ def test_wide_logit_range(sm_scale):
     wl = _wl.small([9000, 3000, 130, 40000], [8, 1, 4, 2], needles=2, seed=61)
     wl.sm_scale = sm_scale
     _gpu.check_decode(wl)
+
+
+@pytest.mark.parametrize("ctx,rows,seed", [
+    ([9000, 130, 20000, 1, 4500], [1, 2, 1, 1, 2], 71),   # partial last blocks, < 16 blocks, one token
+    ([66000] * 6, [2] * 6, 72),
+    ([3000, 500], [0, 2], 73),                              # a request without rows
+])
+def test_small_rows_attention_matches_oracle(ctx, rows, seed):
+    """msa_sparse_attn_decode_small_rows (warp-level MMAs, at most 16 query rows per group)
+    on the oracle's block ids: the path's output and lse bounds."""
+    wl = _wl.small(ctx, rows, needles=2, seed=seed)
+    r = oracle.decode(wl)
+    dec = _gpu.decoder(wl)
+    ids = torch.from_numpy(np.ascontiguousarray(r["ids"])).cuda()
+    out = dec.sparse_attn_small_rows(ids).float().cpu().numpy()
+    lse = dec.lse.cpu().numpy()
+    torch.cuda.synchronize()
+    assert dec.errors() == 0
+    for b in range(wl.num_reqs):
+        r0, r1 = int(wl.q_indptr[b]), int(wl.q_indptr[b + 1])
+        if r1 > r0:
+            _gpu.assert_out_close(out[r0:r1], r["out"][r0:r1], f"request {b}")
+            np.testing.assert_allclose(lse[r0:r1], r["lse"][r0:r1], atol=1e-3, rtol=1e-4)
+
+
+def test_small_rows_attention_flags_and_limits():
+    wl = _wl.small([9000, 5000], [1, 1], seed=74)
+    r = oracle.decode(wl)
+    dec = _gpu.decoder(wl)
+    ids = np.ascontiguousarray(r["ids"]).copy()
+    ids[1, 2, 3] = 10_000  # outside request 1's context
+    dec.sparse_attn_small_rows(torch.from_numpy(ids).cuda())
+    torch.cuda.synchronize()
+    assert dec.errors() & _lib.FLAG_BAD_IDS
+    out = dec.out.float().cpu().numpy()
+    _gpu.assert_out_close(out[0:1], r["out"][0:1], "request 0")  # the other request is untouched
+    wl3 = _wl.small([3000], [3], seed=75)  # 24 query rows: not this path's shape
+    dec3 = _gpu.decoder(wl3)
+    with pytest.raises(MSAError) as e:
+        dec3.sparse_attn_small_rows(dec3.block_ids)
+    assert e.value.code == -2
