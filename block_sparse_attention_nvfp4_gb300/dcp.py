@@ -93,6 +93,7 @@ class DCPSelector:
         if not 1 <= self.world <= MAX_WORLD:
             raise ValueError(f"world {self.world} outside 1..{MAX_WORLD}")
         self.groups = owned_groups(self.rank, self.world, mode)
+        self.cache, self.batch = cache, batch  # the args below hold raw pointers into them
         self.args = _lib.make_args(cache, batch, sm_scale if sm_scale is not None else 128 ** -0.5)
         dev = batch.q_idx.device
         self.ws = torch.empty(_lib.msa_workspace_size(self.args), dtype=torch.uint8, device=dev)

@@ -234,3 +234,29 @@ def test_dcp_rejects_bad_rank_arguments():
     for world, g0, ng in ((0, 0, 4), (9, 0, 4), (2, 3, 2), (2, 0, 0)):
         with pytest.raises(_lib.MSAError):
             _lib.msa_dcp_merge_topk(args, world, g0, ng, k.view(1, 4, 1, 16), ids, ws)
+
+
+@pytest.mark.gpu
+@gpu
+@pytest.mark.parametrize("mode", ["gather", "owner"])
+def test_dcp_selector_through_nccl_single_rank(mode):
+    """dcp.DCPSelector end to end (local step, NCCL exchange, merge) in a one-rank group:
+    the ids equal msa_select_blocks'."""
+    import socket
+    import torch.distributed as dist
+    if not dist.is_nccl_available():
+        pytest.skip("NCCL not available")
+    wl = WORKLOADS["mixed"]()
+    ids, _ = single_gpu(wl)
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        sel = dcp.DCPSelector(KVCache.from_host(wl), DecodeBatch.from_host(wl), mode=mode, sm_scale=wl.sm_scale)
+        got = sel.select().cpu().numpy()
+        torch.cuda.synchronize()
+        assert sel.errors() == 0
+        assert np.array_equal(got, ids)
+    finally:
+        dist.destroy_process_group()
