@@ -478,13 +478,18 @@ msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t*
   if ((s = carve(args, ws, ws_bytes, &w)) != MSA_OK) return s;
   // the index scan with its block max pool, then the attention, chained by programmatic
   // dependent launch. The top-k runs in a kernel of its own between them (one CTA per
-  // request), except when requests may exceed 1,025 blocks and the attention splits each
-  // (request, group) over 4 or more CTAs: then each CTA of the (request, group)'s cluster
-  // ranks a share of the candidates inside the attention kernel and the cluster merges the
-  // shares (measured on GB300: one 524,288-token request 45.5 -> 42-43 us per step; batches
-  // with one or two splits, e.g. 16 x 131,072 or 64 ragged requests, are faster with the kernel)
+  // request), except (measured on GB300) in two cases where the attention kernel ranks its
+  // group's candidates itself, saving a kernel boundary:
+  //  * requests may exceed 1,025 blocks and the attention splits each (request, group) over
+  //    4 or more CTAs: each CTA of the cluster ranks a share of the candidates and the cluster
+  //    merges the shares (one 524,288-token request: 45.5 -> 42-43 us per step);
+  //  * every (request, group) is one CTA and no request exceeds 1,025 blocks: the CTA ranks
+  //    its group's candidates alone (32 x 65,536 tokens: ~80 -> ~78.5 us per step).
+  // Batches with two splits (16 x 131,072) or longer rows in one CTA (64 ragged requests up
+  // to 262,144 tokens) are faster with the kernel.
   const Plan plan = make_plan(args->num_reqs, args->max_rows_per_req, sms);
-  const bool fused_topk = args->max_pages_per_req > 1025 && plan.splits >= 4;
+  const bool fused_topk = (args->max_pages_per_req > 1025 && plan.splits >= 4) ||
+                          (args->max_pages_per_req <= 1025 && plan.splits == 1);
   if ((s = launch_selection(args, 0, block_ids, nullptr, nullptr, 0, w.flags, w.block_S, sms, st, !fused_topk)) !=
       MSA_OK)
     return s;

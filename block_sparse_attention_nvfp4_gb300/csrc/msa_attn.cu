@@ -75,6 +75,7 @@ constexpr int kAttnStages = 4;
 constexpr int kKBufs = 2;                           // dequantised K tiles (free once S is computed)
 constexpr int kVBufs = 3;                           // dequantised V tiles (free once P V is computed)
 constexpr int kSets = 2;                            // softmax sets: set s takes blocks j = s (mod 2)
+constexpr int kMaxSplits = kTopK / 2;               // CTAs per (request, group): at least 2 blocks each
 constexpr uint32_t kHeadPageBytes = kBlock * 64;    // codes of one (page, KV head)
 constexpr uint32_t kHeadScaleBytes = kBlock * 8;
 constexpr uint32_t kTileBytes = kBlock * kDim;      // one dequantised K tile (E4M3, 128-byte rows)
@@ -179,146 +180,9 @@ __device__ __forceinline__ void dq_chunk_v(uint32_t lut_t, const uint4& v, uint3
 
 // Scratch of the fused top-k (in the first K tile, free until block 0 is dequantised).
 struct TopkScratch {
-  uint64_t lm[128];        // the four warps' per-thread maximum keys
-  uint64_t tq[4];          // per-warp threshold candidates
-  uint64_t surv[64];       // candidates at or above the threshold
-  uint64_t all[8][kTopK];  // the cluster's lists, gathered by warp 0
-  int cnt;
+  uint64_t lists[4 * kTopK];  // the four warps' lists (quad_best15)
+  uint64_t surv[4 * 64];      // their survivors
 };
-
-// The 15 best candidates c in [lo, hi) of one group's block scores S (ranking keys: score,
-// then lower id), descending, into out[0..14] (0 where there are fewer), by the 128 threads
-// t = 0..127 of warps 0..3 (named barrier 2). Same threshold idea as the top-k kernel: T =
-// the largest per-thread maximum that at least 15 per-thread maxima reach is at most the
-// 15th best (the 15 largest per-thread maxima are 15 distinct candidates), so the candidates
-// with key >= T contain the answer; they are ranked by counting, or, should more than 64
-// survive, warp 0 merges the whole range exactly by insertion. Ranges of up to 1,024
-// candidates are read once into registers (thread t: candidates lo + 8t .. lo + 8t + 7);
-// longer ones are streamed twice.
-__device__ __noinline__ void range_top15(const float* S, int lo, int hi, TopkScratch& tk, uint64_t* out) {
-  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  constexpr int L = kTopK - 1;
-  const bool direct = hi - lo <= 8 * 128;
-  uint64_t k8[8];
-  uint64_t mx = 0ull;
-  if (direct) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = lo + 8 * t + u;
-      v[u] = c < hi ? __ldcg(S + c) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = lo + 8 * t + u;
-      k8[u] = c < hi ? topk_key(v[u], c) : 0ull;
-      mx = k8[u] > mx ? k8[u] : mx;
-    }
-  } else {
-    for (int c0 = lo; c0 < hi; c0 += 4 * 128) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + t + 128 * u;
-        v[u] = c < hi ? __ldcg(S + c) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + t + 128 * u;
-        if (c < hi) {
-          const uint64_t k = topk_key(v[u], c);
-          mx = k > mx ? k : mx;
-        }
-      }
-    }
-  }
-  tk.lm[t] = mx;
-  if (t == 0) tk.cnt = 0;
-  named_bar_sync(2, 128);
-  int ge = 0;
-#pragma unroll 8
-  for (int j = 0; j < 128; ++j) ge += tk.lm[j] >= mx ? 1 : 0;
-  uint64_t T = (ge >= L && mx != 0ull) ? mx : 0ull;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const uint64_t o = shfl_xor_u64(T, off);
-    T = o > T ? o : T;
-  }
-  if (lane == 0) tk.tq[w] = T;
-  named_bar_sync(2, 128);
-  T = tk.tq[0];
-#pragma unroll
-  for (int q = 1; q < 4; ++q) T = tk.tq[q] > T ? tk.tq[q] : T;
-  auto keep_key = [&](uint64_t key, bool valid) {
-    const bool keep = valid && key >= T;
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-    if (bal != 0u) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&tk.cnt, __popc(bal));
-      base = __shfl_sync(0xFFFFFFFFu, base, 0);
-      const int pos = base + __popc(bal & ((1u << lane) - 1u));
-      if (keep && pos < 64) tk.surv[pos] = key;
-    }
-  };
-  if (direct) {
-#pragma unroll
-    for (int u = 0; u < 8; ++u) keep_key(k8[u], k8[u] != 0ull);
-  } else {
-    for (int c0 = lo; c0 < hi; c0 += 4 * 128) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + t + 128 * u;
-        v[u] = c < hi ? __ldcg(S + c) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + t + 128 * u;
-        keep_key(topk_key(v[u], c), c < hi);
-      }
-    }
-  }
-  named_bar_sync(2, 128);
-  const int count = tk.cnt;
-  if (count <= 64) {
-    for (int i = t; i < count; i += 128) {
-      const uint64_t key = tk.surv[i];
-      int rank = 0;
-      for (int j = 0; j < count; ++j) rank += tk.surv[j] > key ? 1 : 0;
-      if (rank < L) out[rank] = key;
-    }
-    if (t >= count && t < L) out[t] = 0ull;
-  } else if (w == 0) {
-    // exact: per-lane sorted lists of 15 over the whole range, then a 15-round merge
-    uint64_t list[L];
-#pragma unroll
-    for (int j = 0; j < L; ++j) list[j] = 0ull;
-    for (int c = lo + lane; c < hi; c += 32) {
-      const uint64_t key = topk_key(__ldcg(S + c), c);
-      if (key > list[L - 1]) {
-#pragma unroll
-        for (int j = L - 1; j > 0; --j) list[j] = (key > list[j - 1]) ? list[j - 1] : ((key > list[j]) ? key : list[j]);
-        list[0] = key > list[0] ? key : list[0];
-      }
-    }
-#pragma unroll 1
-    for (int k = 0; k < L; ++k) {
-      uint64_t best = list[0];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = shfl_xor_u64(best, off);
-        best = o > best ? o : best;
-      }
-      if (best != 0ull && list[0] == best) {  // keys are unique per block id: exactly one lane
-#pragma unroll
-        for (int j = 0; j < L - 1; ++j) list[j] = list[j + 1];
-        list[L - 1] = 0ull;
-      }
-      if (lane == 0) out[k] = best;
-    }
-  }
-  named_bar_sync(2, 128);
-}
 
 }  // namespace
 
@@ -440,33 +304,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else {
       const int nc = nb - 1;
       const float* Sg = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
-      if (warp < 4) range_top15(Sg, rank * nc / S, (rank + 1) * nc / S, tk, sm.tk_local);
+      if (warp < 4) {
+        const uint64_t best = quad_best15(Sg, rank * nc / S, (rank + 1) * nc / S, warp, 2, tk.lists, tk.surv);
+        if (warp == 0 && lane < kTopK) sm.tk_local[lane] = best;  // descending, zero past the end
+      }
       __syncthreads();
       if (S > 1) cluster_sync_all();  // every CTA's list is in place
       if (warp == 0) {
-        // gather the S lists (local or in the other CTAs' shared memory), then 15 rounds of
-        // taking the largest head
-        const uint32_t local_addr = smem_u32(sm.tk_local);
-        for (int i = lane; i < S * kTopK; i += 32) {
-          const int src = i / kTopK, k = i % kTopK;
-          tk.all[src][k] = k < kTopK - 1 ? (S > 1 ? ld_cluster_u64(cluster_map(local_addr + 8u * k, src))
-                                                  : sm.tk_local[k])
-                                         : 0ull;
-        }
-        __syncwarp();
-        int ptr = 0;
-        int32_t win = nb - 1;  // lane 15 keeps the recent block
-        for (int k = 0; k < kTopK - 1; ++k) {
-          uint64_t head = (lane < S && ptr < kTopK - 1) ? tk.all[lane][ptr] : 0ull;
-          uint64_t best = head;
+        // the S lists (this CTA's, or in the other CTAs' shared memory), all loads issued
+        // first, merged into the 15 best; the ranges are disjoint, so the keys are distinct
+        const uint32_t laddr = smem_u32(sm.tk_local) + 8u * static_cast<uint32_t>(lane & (kTopK - 1));
+        uint64_t kin[kMaxSplits];
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = shfl_xor_u64(best, off);
-            best = o > best ? o : best;
-          }
-          if (lane < S && head == best) ++ptr;  // keys are unique: one lane
-          if (lane == k) win = topk_id(best);
-        }
+        for (int src = 0; src < kMaxSplits; ++src)
+          kin[src] = (src < S && lane < kTopK)
+                         ? (S > 1 ? ld_cluster_u64(cluster_map(laddr, static_cast<uint32_t>(src))) : sm.tk_local[lane])
+                         : 0ull;
+        uint64_t top = kin[0];
+#pragma unroll
+        for (int src = 1; src < kMaxSplits; ++src)
+          if (src < S) top = top32_union(top, kin[src]);
+        const int win = lane < kTopK - 1 ? topk_id(top) : nb - 1;  // lane 15 keeps the recent block
         // the 16 ids ascending
         int r = 0;
 #pragma unroll

@@ -445,6 +445,156 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
   return v;
 }
 
+// Descending order of a bitonic sequence held one value per lane (half-cleaners only).
+__device__ __forceinline__ uint64_t warp_bitonic_merge_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = shfl_xor_u64(v, j);
+    const bool lower = (lane & j) == 0;
+    v = lower ? (o > v ? o : v) : (o < v ? o : v);
+  }
+  return v;
+}
+
+// The 32 largest of two descending lists (one value per lane), descending: the larger of
+// a[i] and b[31 - i] over all i are those 32 values, and they form a bitonic sequence.
+__device__ __forceinline__ uint64_t top32_union(uint64_t a, uint64_t b) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t r = shfl_u64(b, 31 - lane);
+  return warp_bitonic_merge_desc(a > r ? a : r);
+}
+
+// Keys of candidates c0 .. c1-1 of S (block scores an earlier kernel or another CTA wrote:
+// loads bypass L1), id field = candidate index; batch `base` gives lane l the candidates
+// c0 + base + 32u + l, u < 8. All 8 loads are issued before the keys are formed.
+__device__ __forceinline__ void load_keys8(const float* S, int c0, int c1, int base, uint64_t (&k)[8]) {
+  const int lane = threadIdx.x & 31;
+  float v[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int c = c0 + base + 32 * u + lane;
+    v[u] = c < c1 ? __ldcg(S + c) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int c = c0 + base + 32 * u + lane;
+    k[u] = c < c1 ? topk_key(v[u], c) : 0ull;
+  }
+}
+
+// Gather the keys >= T of one batch into surv (up to 64), counting all of them.
+__device__ __forceinline__ void keep_survivors(const uint64_t (&k)[8], uint64_t T, uint64_t* surv, int& count) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const bool keep = k[u] != 0ull && k[u] >= T;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
+    const int pos = count + __popc(bal & ((1u << lane) - 1u));
+    if (keep && pos < 64) surv[pos] = k[u];
+    count += __popc(bal);
+  }
+}
+
+// [vLLM-zh §How; MSA-fig §1 TopK] The 15 largest keys of candidates c0 .. c1-1 by one
+// warp, descending: lane i < 15 returns the i-th (0 past the end). The 15th largest lane
+// maximum T is at most the 15th largest key (the 15 largest lane maxima are 15 distinct
+// candidates), so the keys >= T hold the answer; they are gathered (up to 64; scratch
+// surv) and sorted. If more than 64 pass (ties), the candidates >= T are merged 32 at a
+// time into a running top 32 instead. Ranges of at most 256 candidates are read once,
+// into registers; longer ones are streamed twice.
+static __device__ __noinline__ uint64_t warp_best15(const float* S, int c0, int c1, uint64_t* surv) {
+  constexpr int L = kTopK - 1;
+  const int lane = threadIdx.x & 31;
+  const int n = c1 - c0;
+  uint64_t lmax = 0ull;
+  uint64_t kr[8];
+  if (n <= 256) {
+    load_keys8(S, c0, c1, 0, kr);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) lmax = kr[u] > lmax ? kr[u] : lmax;
+  } else {
+    for (int base = 0; base < n; base += 256) {
+      uint64_t k[8];
+      load_keys8(S, c0, c1, base, k);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lmax = k[u] > lmax ? k[u] : lmax;
+    }
+  }
+  const uint64_t T = shfl_u64(warp_sort_desc(lmax), L - 1);
+  int count = 0;
+  if (n <= 256) {
+    keep_survivors(kr, T, surv, count);
+  } else {
+    for (int base = 0; base < n; base += 256) {
+      uint64_t k[8];
+      load_keys8(S, c0, c1, base, k);
+      keep_survivors(k, T, surv, count);
+    }
+  }
+  __syncwarp();
+  uint64_t top;
+  if (count <= 32) {
+    top = warp_sort_desc(lane < count ? surv[lane] : 0ull);
+  } else if (count <= 64) {
+    const uint64_t a = warp_sort_desc(surv[lane]);
+    const uint64_t b = warp_sort_desc(lane + 32 < count ? surv[lane + 32] : 0ull);
+    top = top32_union(a, b);
+  } else {
+    top = 0ull;
+    for (int base = 0; base < n; base += 256) {
+      uint64_t k[8];
+      if (n <= 256) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) k[u] = kr[u];
+      } else {
+        load_keys8(S, c0, c1, base, k);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t kk = k[u] >= T ? k[u] : 0ull;
+        if (__any_sync(0xFFFFFFFFu, kk != 0ull)) top = top32_union(top, warp_sort_desc(kk));
+      }
+    }
+  }
+  __syncwarp();
+  return lane < L ? top : 0ull;
+}
+
+// The 15 best keys of candidates lo .. hi-1 of S by four warps q = 0..3 (128 threads
+// meeting at named barrier bar_id): warp q takes a quarter with warp_best15 and warp 0
+// merges the four lists (each the exact best 15 of its quarter, so their union holds the
+// best 15 of the range). Returns the i-th best key on lane i < 15 of warp 0 (0 past the
+// end and on the other warps). Scratch: lists [4][16], surv [4][64].
+__device__ __forceinline__ uint64_t quad_best15(const float* S, int lo, int hi, int q, int bar_id, uint64_t* lists,
+                                                uint64_t* surv) {
+  const int lane = threadIdx.x & 31;
+  const int n = hi - lo;
+  const int a = lo + q * n / 4, b = lo + (q + 1) * n / 4;
+  const uint64_t k = warp_best15(S, a, b, surv + 64 * q);
+  if (lane < kTopK) lists[kTopK * q + lane] = k;
+  named_bar_sync(bar_id, 128);
+  if (q != 0) return 0ull;
+  uint64_t top = lane < kTopK ? lists[lane] : 0ull;
+#pragma unroll
+  for (int w = 1; w < 4; ++w) top = top32_union(top, lane < kTopK ? lists[kTopK * w + lane] : 0ull);
+  return lane < kTopK - 1 ? top : 0ull;
+}
+
+// The selection of one group from its 15 best candidate keys (one per lane i < 15 of a
+// warp, nonzero) and the recent block nb - 1: the 16 ids ascending into ids_out.
+__device__ __forceinline__ void write_selection(uint64_t best, int nb, int32_t* ids_out) {
+  const int lane = threadIdx.x & 31;
+  const int my_id = lane < kTopK - 1 ? topk_id(best) : nb - 1;
+  int rank = 0;
+#pragma unroll
+  for (int j = 0; j < kTopK; ++j) {
+    const int other = __shfl_sync(0xFFFFFFFFu, my_id, j);
+    rank += other < my_id ? 1 : 0;
+  }
+  if (lane < kTopK) ids_out[rank] = my_id;
+}
+
 // Score loads of the top-k: plain loads (scores in shared memory, or written by
 // this CTA), or loads that bypass L1 (scores an earlier kernel wrote).
 template <bool kL2>

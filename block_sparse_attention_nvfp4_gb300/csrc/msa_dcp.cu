@@ -29,127 +29,14 @@ constexpr int kCand = kTopK - 1;  // 15 candidates per list
 constexpr int kSlots = kTopK;     // list row: 16 keys = 128 bytes
 constexpr int kDcpThreads = 32 * 4 * kGroups;  // four warps per group
 
-// Descending order of a bitonic sequence held one value per lane (half-cleaners only).
-__device__ __forceinline__ uint64_t warp_bitonic_merge_desc(uint64_t v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 16; j > 0; j >>= 1) {
-    const uint64_t o = shfl_xor_u64(v, j);
-    const bool lower = (lane & j) == 0;
-    v = lower ? (o > v ? o : v) : (o < v ? o : v);
-  }
-  return v;
-}
-
-// The 32 largest of two descending lists (one value per lane), descending: the larger of
-// a[i] and b[31 - i] over all i are those 32 values, and they form a bitonic sequence.
-__device__ __forceinline__ uint64_t top32_union(uint64_t a, uint64_t b) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t r = shfl_u64(b, 31 - lane);
-  return warp_bitonic_merge_desc(a > r ? a : r);
-}
-
-// Keys of candidates c0 .. c1-1 of S (block scores an earlier kernel wrote: loads bypass
-// L1), id field = candidate index; batch `base` gives lane l the candidates
-// c0 + base + 32u + l, u < 8. All 8 loads are issued before the keys are formed.
-__device__ __forceinline__ void load_keys8(const float* S, int c0, int c1, int base, uint64_t (&k)[8]) {
-  const int lane = threadIdx.x & 31;
-  float v[8];
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int c = c0 + base + 32 * u + lane;
-    v[u] = c < c1 ? __ldcg(S + c) : 0.f;
-  }
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int c = c0 + base + 32 * u + lane;
-    k[u] = c < c1 ? topk_key(v[u], c) : 0ull;
-  }
-}
-
-// Gather the keys >= T of one batch into surv (up to 64), counting all of them.
-__device__ __forceinline__ void keep_survivors(const uint64_t (&k)[8], uint64_t T, uint64_t* surv, int& count) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const bool keep = k[u] != 0ull && k[u] >= T;
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-    const int pos = count + __popc(bal & ((1u << lane) - 1u));
-    if (keep && pos < 64) surv[pos] = k[u];
-    count += __popc(bal);
-  }
-}
-
-// The 15 largest keys of candidates c0 .. c1-1, descending: lane i < 15 returns the i-th
-// (0 past the end). The 15th largest lane maximum T is at most the 15th largest key, so
-// the keys >= T hold the answer; they are gathered (up to 64) and sorted. If more than 64
-// pass, the candidates are merged 32 at a time into a running top 32 instead. Ranges of
-// at most 256 candidates are read once, into registers; longer ones are streamed twice.
-__device__ uint64_t warp_best15(const float* S, int c0, int c1, uint64_t* surv) {
-  const int lane = threadIdx.x & 31;
-  const int n = c1 - c0;
-  uint64_t lmax = 0ull;
-  uint64_t kr[8];
-  if (n <= 256) {
-    load_keys8(S, c0, c1, 0, kr);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) lmax = kr[u] > lmax ? kr[u] : lmax;
-  } else {
-    for (int base = 0; base < n; base += 256) {
-      uint64_t k[8];
-      load_keys8(S, c0, c1, base, k);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) lmax = k[u] > lmax ? k[u] : lmax;
-    }
-  }
-  const uint64_t T = shfl_u64(warp_sort_desc(lmax), kCand - 1);
-  int count = 0;
-  if (n <= 256) {
-    keep_survivors(kr, T, surv, count);
-  } else {
-    for (int base = 0; base < n; base += 256) {
-      uint64_t k[8];
-      load_keys8(S, c0, c1, base, k);
-      keep_survivors(k, T, surv, count);
-    }
-  }
-  __syncwarp();
-  uint64_t top;
-  if (count <= 32) {
-    top = warp_sort_desc(lane < count ? surv[lane] : 0ull);
-  } else if (count <= 64) {
-    const uint64_t a = warp_sort_desc(surv[lane]);
-    const uint64_t b = warp_sort_desc(lane + 32 < count ? surv[lane + 32] : 0ull);
-    top = top32_union(a, b);
-  } else {
-    top = 0ull;
-    for (int base = 0; base < n; base += 256) {
-      uint64_t k[8];
-      if (n <= 256) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) k[u] = kr[u];
-      } else {
-        load_keys8(S, c0, c1, base, k);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint64_t kk = k[u] >= T ? k[u] : 0ull;
-        if (__any_sync(0xFFFFFFFFu, kk != 0ull)) top = top32_union(top, warp_sort_desc(kk));
-      }
-    }
-  }
-  __syncwarp();
-  return lane < kCand ? top : 0ull;
-}
-
 // Rank-local lists, after the scan of the rank's blocks (chained to it by programmatic
 // dependent launch): one CTA per request, four warps per group, warp q of group g taking
 // a quarter of the group's candidates; the group's warp 0 merges the four quarter lists
 // (each the exact best 15 of its quarter, so their union holds the group's best 15).
 // block_S column i holds the score of logical block i * world + rank.
 __global__ void __launch_bounds__(kDcpThreads) dcp_local_kernel(const SelectParams p, uint64_t* keys) {
-  __shared__ uint64_t surv[kGroups][4][64];
-  __shared__ uint64_t lists[kGroups][4][kSlots];
+  __shared__ uint64_t surv[kGroups][4 * 64];
+  __shared__ uint64_t lists[kGroups][4 * kTopK];
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = warp >> 2, q = warp & 3;
   const int N = p.context_lens[b];
@@ -161,16 +48,9 @@ __global__ void __launch_bounds__(kDcpThreads) dcp_local_kernel(const SelectPara
   // the recent block (nb - 1) is kept by the merge and is no candidate
   const int nc = nb > 0 && (nb - 1) % p.nshards == p.shard ? nloc - 1 : nloc;
   pdl_wait_primary();  // the block scores come from the scan
-  const int c0 = q * nc / 4, c1 = (q + 1) * nc / 4;
-  uint64_t k = 0ull;
-  if (c1 > c0) k = warp_best15(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride, c0, c1, surv[g][q]);
-  if (lane < kSlots) lists[g][q][lane] = k;
-  named_bar_sync(1 + g, 128);
+  uint64_t k = quad_best15(p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride, 0, nc > 0 ? nc : 0,
+                           q, 1 + g, lists[g], surv[g]);
   if (q != 0) return;
-  uint64_t top = lane < kSlots ? lists[g][0][lane] : 0ull;
-#pragma unroll
-  for (int w = 1; w < 4; ++w) top = top32_union(top, lane < kSlots ? lists[g][w][lane] : 0ull);
-  k = lane < kCand ? top : 0ull;
   if (k != 0ull) {  // candidate index i -> logical block i * world + rank
     const uint32_t id = static_cast<uint32_t>(topk_id(k) * p.nshards + p.shard);
     k = (k & 0xFFFFFFFF00000000ull) | static_cast<uint64_t>(0xFFFFFFFFu - id);

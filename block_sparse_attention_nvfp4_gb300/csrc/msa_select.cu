@@ -621,108 +621,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   (void)all_alive;
 }
 
-// Top-(kTopK-1) of one group's candidates (every block but the recent one) plus the
-// recent block, by the four warps q = 0..3 of the group, scores staged in shared memory
-// [vLLM-zh §How; MSA-fig §1 TopK]. Same ranking key and result as warp_topk. Warp q
-// takes a quarter of the candidates and publishes the 15 largest of its lane maxima;
-// the 15th largest of all lane maxima, T, is at most the group's 15th best (the 15
-// largest lane maxima are 15 distinct candidates), so the candidates with key >= T
-// contain the answer (measured on the synthetic workloads: 15 to 19 of them). The
-// warps collect those survivors and warp 0 sorts them (a rank pass up to 64; should
-// more survive, the exact insertion merge over all candidates).
-__device__ __forceinline__ void group_topk(const float* S, int nb, int32_t* ids_out, int q, int bar_id,
-                                           uint64_t* tq, uint64_t* surv, int* cnt, int32_t* sel) {
-  const int lane = threadIdx.x & 31;
-  constexpr int L = kTopK - 1;
-  if (nb <= kTopK) {
-    if (q == 0 && lane < kTopK) ids_out[lane] = lane < nb ? lane : -1;
-    return;
-  }
-  const int nc = nb - 1;
-  const int n4 = (nc + 3) / 4;  // 16-byte chunks holding the candidates
-  const int a4 = q * n4 / 4, b4 = (q + 1) * n4 / 4;
-  uint64_t lmax = 0ull;
-  for (int c4 = a4 + lane; c4 < b4; c4 += 32) {
-    const float4 v = *reinterpret_cast<const float4*>(S + 4 * c4);
-    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (4 * c4 + t < nc) {
-        const uint64_t k = topk_key(e[t], 4 * c4 + t);
-        lmax = k > lmax ? k : lmax;
-      }
-  }
-  const uint64_t sorted = warp_sort_desc(lmax);
-  if (lane < L) tq[q * L + lane] = sorted;
-  if (q == 0 && lane == 0) *cnt = 0;
-  named_bar_sync(bar_id, 128);
-  // T = the largest published value with at least 15 published values >= it
-  uint64_t T = 0ull;
-  for (int i = lane; i < 4 * L; i += 32) {
-    const uint64_t v = tq[i];
-    int ge = 0;
-    for (int j = 0; j < 4 * L; ++j) ge += tq[j] >= v ? 1 : 0;
-    if (ge >= L && v > T) T = v;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const uint64_t o = shfl_xor_u64(T, off);
-    T = o > T ? o : T;
-  }
-  for (int c40 = a4; c40 < b4; c40 += 32) {
-    const int c4 = c40 + lane;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c4 < b4) v = *reinterpret_cast<const float4*>(S + 4 * c4);
-    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int c = 4 * c4 + t;
-      const uint64_t key = topk_key(e[t], c);
-      const bool keep = c4 < b4 && c < nc && key >= T;
-      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, keep);
-      if (bal != 0u) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(cnt, __popc(bal));
-        base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        if (keep && pos < 64) surv[pos] = key;
-      }
-    }
-  }
-  named_bar_sync(bar_id, 128);
-  if (q != 0) return;
-  const int count = *cnt;
-  if (count > 64) {
-    topk_by_insertion<false>(S, nc, sel);
-  } else if (count <= 32) {
-    const uint64_t k = warp_sort_desc(lane < count ? surv[lane] : 0ull);
-    if (lane < L) sel[lane] = topk_id(k);
-    __syncwarp();
-  } else {
-    for (int i = lane; i < count; i += 32) {
-      const uint64_t k = surv[i];
-      int rank = 0;
-      for (int j = 0; j < count; ++j) rank += surv[j] > k ? 1 : 0;
-      if (rank < L) sel[rank] = topk_id(k);
-    }
-    __syncwarp();
-  }
-  // the 15 winners plus the recent block, ascending
-  const int my_id = lane < L ? sel[lane] : nb - 1;
-  int rank = 0;
-#pragma unroll
-  for (int j = 0; j < kTopK; ++j) {
-    const int other = __shfl_sync(0xFFFFFFFFu, my_id, j);
-    rank += (other < my_id) ? 1 : 0;
-  }
-  if (lane < kTopK) ids_out[rank] = my_id;
-}
-
-// group_topk for requests of at most 32 * 4 * 8 + 1 blocks, straight from the scores in
-// global memory (read past L1; no staging): lane l of warp q holds candidates
-// 256 q + 8 l .. + 7 in registers. T = the largest lane maximum with at least 15 lane
-// maxima at or above it, found by rank counting (no sort); the survivors (15 to 19 on the
-// synthetic workloads) are ranked by counting, and the 16 ids ordered the same way. Same
+// The top-k of one group by its four warps q = 0..3 for requests of at most 32 * 4 * 8 + 1
+// blocks, straight from the scores in global memory (read past L1): lane l of warp q holds
+// candidates 256 q + 8 l .. + 7 in registers. T = the largest lane maximum with at least 15
+// lane maxima at or above it, found by rank counting (no sort); the survivors (15 to 19 on
+// the synthetic workloads) are ranked by counting, and the 16 ids ordered the same way. Same
 // result as warp_topk; more than 32 survivors fall back to the exact insertion merge.
 constexpr int kDirectMax = 32 * 4 * 8;  // candidates (blocks but the recent one)
 __device__ __forceinline__ void group_topk_direct(const float* Sg, int nb, int32_t* ids_out, int q, int bar_id,
@@ -806,15 +709,22 @@ __device__ __forceinline__ void group_topk_direct(const float* Sg, int nb, int32
 // Step 3 of the selection, after the scan: one CTA per request, four warps per group.
 // A kernel of its own so it runs on SMs the scan has left; chained to the scan by
 // programmatic dependent launch, it reads the request geometry before waiting.
+// [vLLM-zh §How; MSA-fig §1 TopK] group g keeps its recent block and the 15 best of the
+// others (score, then lower id); every block when there are at most 16. Up to 1,025 blocks
+// the group's four warps rank by a threshold from their lane maxima (group_topk_direct);
+// longer rows are split in quarters, one per warp (quad_best15), and the group's warp 0
+// merges the quarters. Both read the scores the scan left in L2. (Measured on GB300 in the
+// decode chain: the direct form ~2 us faster at 1,023 candidates, the quarters ~5 us faster
+// on the ragged batch whose longest request has 2,047.)
 constexpr int kTopkThreads = 128 * kGroups;
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p, int stage_row) {
-  extern __shared__ float tk_stage[];  // [4][stage_row] block scores (stage_row = 0: read global)
-  __shared__ uint64_t tq[kGroups][4 * (kTopK - 1)];
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p) {
+  __shared__ uint64_t lists[kGroups][4 * kTopK];
+  __shared__ uint64_t qsurv[kGroups][4 * 64];
   __shared__ uint64_t surv[kGroups][64];
-  __shared__ int cnt[kGroups];
-  __shared__ int32_t sel[kGroups][kTopK];
   __shared__ uint64_t lm[kGroups][128];
   __shared__ uint64_t tmax[kGroups][4];
+  __shared__ int cnt[kGroups];
+  __shared__ int32_t sel[kGroups][kTopK];
   pdl_launch_dependents();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = warp >> 2, q = warp & 3;
@@ -824,57 +734,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const SelectParams p
   const bool ok = N >= 0 && N <= p.max_pages * kBlock && R >= 0 && R <= kMaxRows && R <= N && r0 >= 0 &&
                   r0 + R <= p.total_rows;
   const int nbb = ok && R > 0 ? (N + kBlock - 1) / kBlock : 0;
-  const bool direct = nbb > kTopK && nbb - 1 <= kDirectMax;  // scores read straight into registers
   pdl_wait_primary();  // the block scores come from the scan kernel
-  if (stage_row > 0 && nbb > 0 && !direct) {
-    // stage the request's 4 score rows, issuing every load of a thread before its stores
-    // (one round trip to L2 instead of one per load); loads bypass L1, whose lines may
-    // predate the scan
-    const int row4 = (nbb + 3) / 4, tot = kGroups * row4;
-    const float* rows = p.block_S + static_cast<long long>(b) * kGroups * p.s_stride;
-    for (int u0 = 0; u0 < tot; u0 += kTopkThreads * 4) {
-      float4 v[4];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int u = u0 + t * kTopkThreads + threadIdx.x;
-        const int gg = u / row4, c4 = u - gg * row4;
-        v[t] = u < tot ? __ldcg(reinterpret_cast<const float4*>(rows + static_cast<long long>(gg) * p.s_stride) + c4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int u = u0 + t * kTopkThreads + threadIdx.x;
-        const int gg = u / row4, c4 = u - gg * row4;
-        if (u < tot) reinterpret_cast<float4*>(tk_stage + gg * stage_row)[c4] = v[t];
-      }
-    }
-  }
-  __syncthreads();
   int32_t* ids = p.block_ids + (static_cast<long long>(b) * kGroups + g) * kTopK;
-  float* sout = p.block_scores_out != nullptr
-                    ? p.block_scores_out + (static_cast<long long>(b) * kGroups + g) * p.max_pages
-                    : nullptr;
-  if (nbb == 0) {  // no pages: an empty selection
-    if (q == 0 && lane < kTopK) ids[lane] = -1;
-    if (sout != nullptr)
-      for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = -INFINITY;
-    return;
-  }
-  if (direct) {
-    const float* S = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
+  const float* S = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
+  if (nbb <= kTopK) {  // every block (none: an empty selection)
+    if (q == 0 && lane < kTopK) ids[lane] = lane < nbb ? lane : -1;
+  } else if (nbb - 1 <= kDirectMax) {
     group_topk_direct(S, nbb, ids, q, 1 + g, lm[g], tmax[g], surv[g], &cnt[g], sel[g]);
-    if (sout != nullptr)
-      for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = c < nbb ? __ldcg(S + c) : -INFINITY;
-  } else if (stage_row > 0) {
-    const float* S = tk_stage + g * stage_row;
-    group_topk(S, nbb, ids, q, 1 + g, tq[g], surv[g], &cnt[g], sel[g]);
-    if (sout != nullptr)
-      for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = c < nbb ? S[c] : -INFINITY;
-  } else {  // rows too long to stage: one warp per group reads them past L1
-    const float* S = p.block_S + (static_cast<long long>(b) * kGroups + g) * p.s_stride;
-    if (q == 0) warp_topk<true>(S, nbb, ids, surv[g]);
-    if (sout != nullptr)
-      for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = c < nbb ? __ldcg(S + c) : -INFINITY;
+  } else {
+    const uint64_t best = quad_best15(S, 0, nbb - 1, q, 1 + g, lists[g], qsurv[g]);
+    if (q == 0) write_selection(best, nbb, ids);
+  }
+  if (p.block_scores_out != nullptr) {
+    float* sout = p.block_scores_out + (static_cast<long long>(b) * kGroups + g) * p.max_pages;
+    for (int c = q * 32 + lane; c < p.max_pages; c += 128) sout[c] = c < nbb ? __ldcg(S + c) : -INFINITY;
   }
 }
 
@@ -977,22 +850,16 @@ cudaError_t launch_select(const CUtensorMap& ki_map, const SelectParams& prm, in
 }
 
 cudaError_t launch_topk(const SelectParams& prm, cudaStream_t st) {
-  // stage each group's score row in shared memory when the 4 rows fit in 160 KB
-  const int stage_row = static_cast<size_t>(kGroups) * prm.s_stride * sizeof(float) <= 160 * 1024 ? prm.s_stride : 0;
-  const size_t smem = static_cast<size_t>(kGroups) * stage_row * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.num_reqs, 1, 1);
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_kernel, prm, stage_row);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

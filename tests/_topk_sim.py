@@ -2,14 +2,15 @@
 
 The kernels select the recent block plus the 15 best others by ranking keys
 (score's order-preserving integer image in the high word, the complemented block
-id in the low word: higher score first, then lower id). They first find a
-threshold T no larger than the 15th best key, keep the candidates with key >= T
-(the survivors), and rank those; when too many survive they fall back to an exact
-insertion merge over all candidates. Which ranking branch runs depends only on
-how many survive, so the tests use this model on the GPU's own block scores to
-state which branch each case reaches. It mirrors the candidate-to-lane layout
-and the threshold rule of each kernel form; it is not used to check results
-(the oracle's full sort does that).
+id in the low word: higher score first, then lower id). Each warp ranks a range of
+candidates: it finds a threshold T no larger than the range's 15th best key (the
+15th largest of its lanes' maxima), keeps the candidates with key >= T (the
+survivors) and sorts those, or, when more than 64 survive, merges every candidate
+>= T into a running top 32. Which branch runs depends only on how many survive and
+on the range's length, so the tests use this model on the GPU's own block scores to
+state which branch each case reaches. It mirrors the candidate-to-lane layout and
+the threshold rule of each kernel form; it is not used to check results (the
+oracle's full sort does that).
 """
 import numpy as np
 
@@ -29,14 +30,42 @@ def keys(scores, ids=None):
     return (hi << np.uint64(32)) | lo
 
 
-def _survivors(k, T):
-    return int(np.sum(k >= T))
+def warp_best15(k):
+    """warp_best15 over one warp's candidates (keys in candidate order; candidate i in lane
+    i % 32): T = the 15th largest lane maximum; the candidates >= T survive. Returns
+    (survivors, branch): "sort" (<= 32), "two_sorts" (33..64), "chunked" (> 64, merged 32 at
+    a time), with "/regs" when the warp holds at most 256 candidates (read once into
+    registers) and "/stream" otherwise (read twice)."""
+    lm = np.zeros(32, np.uint64)
+    for i in range(len(k)):
+        lm[i % 32] = max(lm[i % 32], k[i])
+    T = np.sort(lm)[::-1][L - 1]
+    n = int(np.sum((k >= T) & (k != 0)))
+    br = "chunked" if n > 64 else "two_sorts" if n > 32 else "sort"
+    return n, br + ("/regs" if len(k) <= 256 else "/stream")
+
+
+def quad(scores, lo, hi, ids=None):
+    """quad_best15 over candidates lo .. hi-1 (four warps, warp q taking
+    [lo + q n / 4, lo + (q + 1) n / 4), n = hi - lo): the (survivors, branch) of every warp
+    with candidates. ids: the candidates' block ids (default: their index)."""
+    if ids is None:
+        ids = np.arange(len(scores))
+    k = keys(np.asarray(scores)[lo:hi], np.asarray(ids)[lo:hi])
+    n = hi - lo
+    out = []
+    for q in range(4):
+        a, b = q * n // 4, (q + 1) * n // 4
+        if b > a:
+            out.append(warp_best15(k[a:b]))
+    return out
 
 
 def direct(block_scores, nb):
-    """group_topk_direct (requests of 17..1025 blocks): lane l of warp q holds
-    candidates 256q + 8l .. +7; T = the largest lane maximum that at least 15 lane
-    maxima reach. Returns (survivors, branch)."""
+    """group_topk_direct (requests of 17..1025 blocks): lane l of warp q holds candidates
+    256q + 8l .. +7; T = the largest lane maximum that at least 15 lane maxima reach.
+    Returns (survivors, branch): "rank" (<= 32, ranked by counting) or "insertion" (the
+    exact insertion merge)."""
     nc = nb - 1
     k = keys(block_scores[:nc])
     lm = np.zeros(128, np.uint64)
@@ -46,38 +75,24 @@ def direct(block_scores, nb):
             seg = k[c0:min(c0 + 8, nc)]
             lm[32 * q + l] = seg.max() if len(seg) else 0
     T = max((m for m in lm if np.sum(lm >= m) >= L), default=np.uint64(0))
-    n = _survivors(k, T)
+    n = int(np.sum(k >= T))
     return n, ("insertion" if n > 32 else "rank")
 
 
-def staged(block_scores, nb):
-    """group_topk (scores staged in shared memory): warp q takes 16-byte chunks
-    [q n4 / 4, (q + 1) n4 / 4), lane l the chunks a4 + l + 32 j; each warp publishes
-    its 15 largest lane maxima; T = the largest published value that at least 15
-    published values reach."""
-    nc = nb - 1
-    k = keys(block_scores[:nc])
-    n4 = (nc + 3) // 4
-    pub = []
-    for q in range(4):
-        a4, b4 = q * n4 // 4, (q + 1) * n4 // 4
-        lm = np.zeros(32, np.uint64)
-        for l in range(32):
-            for c4 in range(a4 + l, b4, 32):
-                seg = k[4 * c4:min(4 * c4 + 4, nc)]
-                if len(seg):
-                    lm[l] = max(lm[l], seg.max())
-        pub.extend(sorted(lm, reverse=True)[:L])
-    pub = np.array(pub, np.uint64)
-    T = max((v for v in pub if np.sum(pub >= v) >= L), default=np.uint64(0))
-    n = _survivors(k, T)
-    return n, ("insertion" if n > 64 else "rank" if n > 32 else "sort")
+def topk_kernel(block_scores, nb):
+    """The top-k kernel (and the selection call): the (survivors, branch) list of the direct
+    form for up to 1,024 candidates (branch prefixed "direct/"), else of quad over the
+    nb - 1 candidates."""
+    if nb - 1 <= 1024:
+        n, br = direct(block_scores, nb)
+        return [(n, "direct/" + br)]
+    return quad(block_scores, 0, nb - 1)
 
 
 def warp(block_scores, nb):
-    """warp_topk (one warp; rows too long to stage, and the top-k from given token
-    scores): lane l holds the candidates of 16-byte chunks l, l + 32, ...; T = the
-    15th largest lane maximum."""
+    """warp_topk (one warp: the top-k from given token scores): lane l holds the
+    candidates of 16-byte chunks l, l + 32, ...; T = the 15th largest lane maximum.
+    Returns (survivors, branch)."""
     nc = nb - 1
     k = keys(block_scores[:nc])
     lm = np.zeros(32, np.uint64)
@@ -87,19 +102,8 @@ def warp(block_scores, nb):
             if len(seg):
                 lm[l] = max(lm[l], seg.max())
     T = np.sort(lm)[::-1][L - 1]
-    n = _survivors(k, T)
+    n = int(np.sum(k >= T))
     return n, ("insertion" if n > 48 else "rank" if n > 32 else "sort")
-
-
-def kernel_form(nb, max_pages):
-    """Which form the fused top-k kernel uses for a request of nb blocks in a batch
-    whose block-table rows hold max_pages entries."""
-    if nb <= 16:
-        return "all"
-    if nb - 1 <= 1024:
-        return "direct"
-    stride = (max_pages + 3) // 4 * 4
-    return "staged" if 4 * stride * 4 <= 160 * 1024 else "warp"
 
 
 def attention_splits(num_reqs, sm_count):
@@ -115,47 +119,15 @@ def attention_splits(num_reqs, sm_count):
     return 16 // bps
 
 
-def range_top15(block_scores, lo, hi):
-    """The attention kernel's top-k of candidates [lo, hi) for one CTA of a cluster: 128
-    threads; ranges of up to 1,024 candidates held 8 per thread (thread t: lo + 8t ..), longer
-    ones strided (thread t: lo + t + 128 i); T = the largest per-thread maximum that at least
-    15 per-thread maxima reach; more than 64 survivors take the exact insertion merge.
-    Returns (survivors, branch)."""
-    k = keys(block_scores[lo:hi], np.arange(lo, hi))
-    n = hi - lo
-    direct = n <= 1024
-    lm = np.zeros(128, np.uint64)
-    for t in range(128):
-        seg = k[8 * t:8 * t + 8] if direct else k[t::128]
-        lm[t] = seg.max() if len(seg) else 0
-    T = max((m for m in lm if m != 0 and np.sum(lm >= m) >= L), default=np.uint64(0))
-    n_surv = int(np.sum(k >= T))
-    return n_surv, ("insertion" if n_surv > 64 else "rank") + ("/direct" if direct else "/strided")
-
-
 def fused_branches(block_scores, nb, splits):
-    """range_top15's branch on every CTA of a (request, group) cluster of `splits` CTAs."""
+    """The attention kernel's fused top-k: CTA s of a (request, group) cluster of `splits`
+    CTAs runs quad over candidates [s nc / splits, (s + 1) nc / splits); the branches of all
+    warps of all CTAs."""
     nc = nb - 1
-    return [range_top15(block_scores, s * nc // splits, (s + 1) * nc // splits)[1] for s in range(splits)]
+    return [br for s in range(splits) for _, br in quad(block_scores, s * nc // splits, (s + 1) * nc // splits)]
 
 
 def dcp_local(local_scores, nc):
-    """warp_best15 of the DCP rank-local lists: four warps per group, warp q taking the
-    candidates [q nc / 4, (q + 1) nc / 4) (the rank's blocks in order, recent block
-    excluded), candidate c0 + i in lane i % 32; T = the 15th largest lane maximum of the
-    warp. Returns the branch of each warp: "sort" (<= 32 survivors), "two_sorts" (33..64),
-    "chunked" (> 64: the candidates merged 32 at a time)."""
-    k = keys(local_scores[:nc])
-    out = []
-    for q in range(4):
-        c0, c1 = q * nc // 4, (q + 1) * nc // 4
-        if c1 <= c0:
-            continue
-        kq = k[c0:c1]
-        lm = np.zeros(32, np.uint64)
-        for i in range(len(kq)):
-            lm[i % 32] = max(lm[i % 32], kq[i])
-        T = np.sort(lm)[::-1][L - 1]
-        n = int(np.sum((kq >= T) & (kq != 0)))
-        out.append((n, "chunked" if n > 64 else "two_sorts" if n > 32 else "sort"))
-    return out
+    """The DCP rank-local lists: quad over the rank's nc candidates (its blocks in order,
+    recent block excluded). Returns (survivors, branch) of each warp."""
+    return quad(local_scores, 0, nc)

@@ -149,12 +149,12 @@ def test_dcp_equals_single_gpu_selection(name, world):
 # tie-heavy single requests (logical blocks aliased onto a few pages): each reaches the
 # named filter branch of the rank-local list on at least one (rank, group)
 TIES = [
-    (8, 3000, 8, 1, "chunked"),     # quarters of ~750 candidates: streamed, > 64 survivors
-    (8, 5000, 16, 2, "chunked"),    # quarters of ~625: streamed
-    (8, 3000, 8, 4, "chunked"),     # quarters of ~187: held in registers, > 64 survivors
-    (4, 3000, 8, 4, "two_sorts"),   # registers, 33..64 survivors
-    (8, 1100, 1, 2, "two_sorts"),
-    (8, 300, 1, 4, "sort"),
+    (8, 3000, 8, 1, "chunked/stream"),     # quarters of ~750 candidates: streamed, > 64 survivors
+    (8, 5000, 16, 2, "chunked/stream"),    # quarters of ~625: streamed
+    (8, 3000, 8, 4, "chunked/regs"),       # quarters of ~187: held in registers, > 64 survivors
+    (4, 3000, 8, 4, "two_sorts/regs"),     # registers, 33..64 survivors
+    (8, 1100, 1, 2, "two_sorts/regs"),
+    (8, 300, 1, 4, "sort/regs"),
 ]
 
 

@@ -7,10 +7,10 @@ ties on purpose: many logical blocks of a request map, through the block table, 
 a few physical pages. Blocks on the same page get bit-identical block scores on
 both sides (same keys, same queries, exact maxima), so the lower-id rule decides
 the selection, and long runs of equal keys push the kernels' threshold filters
-past their register/shared-memory ranking into their exact fallbacks. Each case
-names the branch it must reach; a host model of the filters (tests/_topk_sim.py)
-computes the branch from the GPU's own block scores, so the claim is checked on
-every run. Ids must equal the oracle's exactly (no near-tie waiver applies to an
+past the sort of their survivors into the merge of two sorted halves and the
+chunked merge of every candidate above the threshold. Each case names the branch it
+must reach; a host model of the filters (tests/_topk_sim.py) computes the branch
+from the GPU's own block scores, so the claim is checked on every run. Ids must equal the oracle's exactly (no near-tie waiver applies to an
 exact tie)."""
 import copy
 
@@ -47,42 +47,42 @@ def aliased(n_pages, nb, run, rows=2, tail=0, max_pages=None, seed=40, zero_inde
     return wl
 
 
-def branches(form, bs, nb):
-    model = {"direct": _topk_sim.direct, "staged": _topk_sim.staged, "warp": _topk_sim.warp}[form]
-    return [model(bs[g], nb) for g in range(4)]
+def branches(bs, nb):
+    """Every (warp, group) branch of the top-k kernel's filter on these block scores."""
+    return {br for g in range(4) for _, br in _topk_sim.topk_kernel(bs[g], nb)}
 
 
-# (pages, blocks, run, max_pages or None, form, branch that at least one group must reach)
+# (pages, blocks, run, max_pages or None, branch that at least one group must reach). Up to
+# 1,025 blocks: the direct form's rank counting (<= 32 survivors) or its exact insertion merge;
+# longer rows: quad_best15's survivor sort (<= 32), two sorted halves (33..64) or chunked merge
+# (> 64), each warp's quarter streamed twice. The last case's block-table rows hold 10,300
+# entries, far more than the request uses.
 CASES = [
-    (8, 300, 1, None, "direct", "rank"),          # <= 32 survivors, ranked by counting
-    (4, 300, 8, None, "direct", "insertion"),     # > 32 survivors: exact insertion merge
-    (3, 1100, 1, None, "staged", "sort"),         # staged rows, <= 32 survivors
-    (4, 1100, 64, None, "staged", "rank"),        # 33..64 survivors
-    (8, 3000, 8, None, "staged", "insertion"),    # > 64 survivors
-    (8, 3000, 1, 10300, "warp", "sort"),          # rows too long to stage: one warp per group
-    (3, 1100, 9, 10300, "warp", "rank"),          # 33..48 survivors
-    (4, 3000, 8, 10300, "warp", "insertion"),     # > 48 survivors
+    (8, 300, 1, None, "direct/rank"),
+    (4, 300, 8, None, "direct/insertion"),
+    (3, 1100, 1, None, "sort/stream"),
+    (8, 1100, 8, None, "two_sorts/stream"),
+    (8, 3000, 1, 10300, "chunked/stream"),
 ]
 
 
 @pytest.mark.gpu
 @gpu
-@pytest.mark.parametrize("pages,nb,run,max_pages,form,branch", CASES)
-def test_fused_topk_ties_and_overflow(pages, nb, run, max_pages, form, branch):
+@pytest.mark.parametrize("pages,nb,run,max_pages,branch", CASES)
+def test_topk_ties_and_overflow(pages, nb, run, max_pages, branch):
     wl = aliased(pages, nb, run, max_pages=max_pages, tail=37)
-    assert _topk_sim.kernel_form(nb, wl.max_pages_per_req) == form
     dec = _gpu.decoder(wl, with_block_scores=True)
     ids = dec.select_blocks().cpu().numpy()
     bs = dec.block_scores.cpu().numpy()
     torch.cuda.synchronize()
     assert dec.errors() == 0
-    got = branches(form, bs[0], nb)
-    assert branch in [b for _, b in got], got
+    got = branches(bs[0], nb)
+    assert branch in got, got
     ref = oracle.decode(wl)
     S = ref["S"][0][:, :nb]
     np.testing.assert_allclose(bs[0, :, :nb], S, rtol=1e-5, atol=1e-4)
     for g in range(4):
-        _gpu.assert_topk_exact_on_own_scores(ids[0, g], bs[0, g], nb, (form, g))
+        _gpu.assert_topk_exact_on_own_scores(ids[0, g], bs[0, g], nb, (branch, g))
         # the page with the best score has many aliases: an exact tie at the boundary
         others = np.sort(S[g, :nb - 1])[::-1]
         assert others[14] == others[15], "the case must put an exact tie at the 15/16 boundary"
@@ -93,9 +93,8 @@ def test_fused_topk_ties_and_overflow(pages, nb, run, max_pages, form, branch):
 
 @pytest.mark.gpu
 @gpu
-@pytest.mark.parametrize("nb,max_pages,form", [(300, None, "direct"), (1100, None, "staged"),
-                                               (1100, 10300, "warp")])
-def test_zero_index_scales_tie_every_block(nb, max_pages, form):
+@pytest.mark.parametrize("nb,max_pages", [(300, None), (1100, None), (1100, 10300)])
+def test_zero_index_scales_tie_every_block(nb, max_pages):
     """An index cache whose scales are all zero scores every token 0: every block
     ties, so the selection is the 15 lowest ids plus the recent block."""
     wl = aliased(4, nb, 1, max_pages=max_pages, zero_index_scales=True)
@@ -112,18 +111,32 @@ def test_zero_index_scales_tie_every_block(nb, max_pages, form):
 
 
 def test_branch_coverage_of_the_cases():
-    """The parametrised cases above reach every ranking branch of every kernel form
-    (checked on the host model over the oracle's block scores, so this runs quickly
-    and states the coverage claim next to the cases)."""
+    """The parametrised cases reach every branch of the top-k kernel's two forms (CASES) and
+    of the attention kernel's fused top-k, register and streamed (FUSED), CASES each with an
+    exact tie at the 15/16 boundary (checked on the host model over the oracle's block
+    scores, so this runs quickly and states the coverage claim next to the cases)."""
+    all_branches = {f"{b}/{p}" for b in ("sort", "two_sorts", "chunked") for p in ("regs", "stream")}
     seen = set()
-    for pages, nb, run, max_pages, form, branch in CASES:
+    for pages, nb, run, max_pages, branch in CASES:
         wl = aliased(pages, nb, run, max_pages=max_pages, tail=37)
         S = oracle.decode(wl)["S"][0][:, :nb].astype(np.float32)
-        seen |= {(form, b) for _, b in branches(form, S, nb)}
-    for form, brs in (("direct", ("rank", "insertion")), ("staged", ("sort", "rank", "insertion")),
-                      ("warp", ("sort", "rank", "insertion"))):
-        for b in brs:
-            assert (form, b) in seen, (form, b, sorted(seen))
+        got = branches(S, nb)
+        assert branch in got, (pages, nb, run, got)
+        seen |= got
+        for g in range(4):
+            others = np.sort(S[g, :nb - 1])[::-1]
+            assert others[14] == others[15], (pages, nb, run, g)
+    assert seen >= {"direct/rank", "direct/insertion", "sort/stream", "two_sorts/stream", "chunked/stream"}, sorted(seen)
+    seen = set()
+    for nreq, pages, nb, run, branch in FUSED:
+        # the page scores of the aliased request (every block but the last fully visible)
+        ps = oracle.decode(aliased(pages, pages + 1, 1, rows=1, seed=41))["S"][0][:, :pages].astype(np.float32)
+        bs = ps[:, (np.arange(nb) // run) % pages]
+        splits = _topk_sim.attention_splits(nreq, 152)  # GB300's SM count
+        got = {br for g in range(4) for br in _topk_sim.fused_branches(bs[g], nb, splits)}
+        assert branch in got, (pages, nb, run, got)
+        seen |= got
+    assert seen >= all_branches, sorted(seen)
 
 
 @pytest.mark.gpu
@@ -176,15 +189,23 @@ def test_signed_zero_scores_tie():
     assert np.array_equal(ids[0, 0], np.array(list(range(15)) + [nb - 1], np.int32))
 
 
-# msa_decode ranks requests of over 1,025 blocks inside its attention kernel when each
+# msa_decode ranks inside its attention kernel (1) requests of over 1,025 blocks when each
 # (request, group) is split over 4 or more CTAs: each CTA of the (request, group)'s cluster
-# ranks a share of the candidates and the cluster merges the shares' 15 best exactly.
-# (requests, pages, blocks, run, ranking branch one CTA must reach)
+# ranks a share of the candidates (quad_best15) and the cluster merges the shares' 15 best
+# exactly (one request: 8 CTAs per (request, group)); (2) requests of at most 1,025 blocks
+# when each (request, group) is one CTA (20 or more requests on 152 SMs): that CTA ranks all
+# of its group's candidates.
+# (requests, pages, blocks, run, branch one warp of one CTA must reach)
 FUSED = [
-    (1, 8, 3000, 8, "rank/direct"),            # 8 CTAs x ~375 candidates
-    (1, 4, 3000, 64, "insertion/direct"),      # long runs of one page in a CTA's share
-    (1, 8, 10000, 1, "rank/strided"),          # 8 CTAs x 1,250 candidates
-    (1, 128, 10000, 1, "insertion/strided"),   # each thread's share holds one page: 15 pages survive
+    (1, 3, 3000, 1, "sort/regs"),             # 8 CTAs x ~375 candidates, ~94 per warp
+    (1, 8, 3000, 1, "two_sorts/regs"),
+    (1, 4, 8193, 8, "chunked/regs"),          # 256 candidates per warp
+    (1, 3, 10000, 1, "sort/stream"),          # ~312 per warp: read twice
+    (1, 8, 10000, 8, "two_sorts/stream"),
+    (1, 4, 10000, 1, "chunked/stream"),
+    (20, 3, 1000, 1, "sort/regs"),            # one CTA per (request, group), ~250 per warp
+    (20, 8, 600, 2, "two_sorts/regs"),
+    (20, 8, 1000, 1, "chunked/regs"),
 ]
 
 
