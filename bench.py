@@ -280,6 +280,9 @@ def measure_dcp(l2_flush, stream, reps, name="long_512k", world=4):
         local_us.append(spread(time_calls(fn, l2_flush, stream, reps))["mean_us"])
     all_keys = torch.stack(keys).contiguous()
     merge = lambda: _lib.msa_dcp_merge_topk(args, world, 0, 4, all_keys, ids, dec.ws)  # noqa: E731
+    for _ in range(3):  # untimed first calls (module loading, first-touch costs)
+        merge()
+        dec.select_blocks()
     merge_us = spread(time_calls(merge, l2_flush, stream, reps))["mean_us"]
     single_us = spread(time_calls(dec.select_blocks, l2_flush, stream, reps))["mean_us"]
     torch.cuda.synchronize()
