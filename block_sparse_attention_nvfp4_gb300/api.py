@@ -106,6 +106,10 @@ class MSADecoder:
         """Pinned host staging for whole decode steps from host memory (see HostIO)."""
         return HostIO(self)
 
+    def host_stream(self, depth: int = 2) -> "HostStream":
+        """Decode steps from host memory with `depth` steps in flight (see HostStream)."""
+        return HostStream(self, depth)
+
     def select_blocks(self, stream=None):
         _lib.msa_select_blocks(self.args, self.block_ids, self.block_scores, self.ws, stream)
         return self.block_ids
@@ -201,16 +205,20 @@ class HostIO:
         launch per step instead of five. If capture is not possible the step runs eagerly
         (`graph_error` says why)."""
         s = stream if stream is not None else torch.cuda.current_stream()
-        if graph and self.graph is None and self.graph_error is None:
-            self._capture()
-        if graph and self.graph is not None:
-            with torch.cuda.stream(s):
-                self.graph.replay()
-        else:
-            with torch.cuda.stream(s):
-                self._enqueue(s)
+        self.launch(s, graph)
         s.synchronize()
         return self.outputs
+
+    def launch(self, stream, graph: bool = True):
+        """Enqueue one step on `stream` without waiting for it (`step` without the
+        synchronize): `outputs` hold its results once the stream has reached that point."""
+        if graph and self.graph is None and self.graph_error is None:
+            self._capture()
+        with torch.cuda.stream(stream):
+            if graph and self.graph is not None:
+                self.graph.replay()
+            else:
+                self._enqueue(stream)
 
     graph = None
     graph_error = None
@@ -234,3 +242,68 @@ class HostIO:
         except Exception as e:  # keep the eager path
             self.graph_error = repr(e)
             torch.cuda.synchronize()
+
+
+class HostStream:
+    """Decode steps from host memory with several in flight: `depth` slots, each its own
+    decoder (sharing the cache), pinned input and output mirrors, device buffers and
+    workspace (HostIO). Step i uses slot i % depth once that slot's previous step has been
+    consumed. Its input copy runs on a copy stream, its three kernels on one compute stream
+    shared by all slots (the steps' kernels never compete for SMs), its output copy on a
+    second copy stream, ordered by events: the copies of one step overlap the kernels of
+    the steps next to it.
+
+    run(steps, fill, consume): for each step, `fill(i, inputs)` writes its inputs into the
+    slot's pinned input views (None: keep what is there), and `consume(i, outputs)` is called
+    with the slot's pinned output views once the step is complete (before the slot is
+    reused, or at the end)."""
+
+    def __init__(self, dec: "MSADecoder", depth: int = 2):
+        if depth < 1:
+            raise ValueError("depth must be at least 1")
+        self.slots = [HostIO(MSADecoder(dec.cache, dec.batch, sm_scale=dec.sm_scale, with_lse=dec.lse is not None))
+                      for _ in range(depth)]
+        self.copy_in, self.compute, self.copy_out = (torch.cuda.Stream() for _ in range(3))
+        self.in_done = [torch.cuda.Event() for _ in range(depth)]
+        self.kernels_done = [torch.cuda.Event() for _ in range(depth)]
+        self.done = [torch.cuda.Event() for _ in range(depth)]
+        self.h2d_bytes = self.slots[0].h2d_bytes
+        self.d2h_bytes = self.slots[0].d2h_bytes
+
+    @property
+    def depth(self) -> int:
+        return len(self.slots)
+
+    def _launch(self, k: int):
+        io = self.slots[k]
+        with torch.cuda.stream(self.copy_in):
+            io.dev_in.copy_(io.host_in, non_blocking=True)
+            self.in_done[k].record(self.copy_in)
+        self.compute.wait_event(self.in_done[k])
+        io.dec.decode(self.compute)
+        self.kernels_done[k].record(self.compute)
+        self.copy_out.wait_event(self.kernels_done[k])
+        with torch.cuda.stream(self.copy_out):
+            io.host_out.copy_(io.dev_out, non_blocking=True)
+            self.done[k].record(self.copy_out)
+
+    def run(self, steps: int, fill=None, consume=None):
+        pending = [None] * self.depth  # the step each slot last ran, until consumed
+        for i in range(steps):
+            k = i % self.depth
+            if pending[k] is not None:
+                self.done[k].synchronize()
+                if consume is not None:
+                    consume(pending[k], self.slots[k].outputs)
+                pending[k] = None
+            if fill is not None:
+                fill(i, self.slots[k].inputs)
+            self._launch(k)
+            pending[k] = i
+        for j in range(steps, steps + self.depth):  # the last steps, in order
+            k = j % self.depth
+            if pending[k] is not None:
+                self.done[k].synchronize()
+                if consume is not None:
+                    consume(pending[k], self.slots[k].outputs)
+                pending[k] = None

@@ -211,6 +211,44 @@ def test_host_io_step_matches_device_decode(ragged):
     assert torch.equal(res["out"], out_ref) and torch.equal(res["lse"], lse_ref)
 
 
+def test_host_stream_steps_in_flight_match_device_decode(ragged):
+    """MSADecoder.host_stream(): steps in flight on separate slots. Alternate steps get two
+    different query sets through the pinned inputs; every step's outputs, read when its slot
+    is reused or at the end, equal the device path's results for the queries that step was
+    given (no slot reads another step's buffers)."""
+    dec = _gpu.decoder(ragged)
+    out_a, ids_a = (t.clone().cpu() for t in dec.decode())
+    lse_a = dec.lse.clone().cpu()
+    q_b = torch.flip(dec.batch.q, dims=[1]).contiguous()        # heads reversed: other queries
+    qi_b = torch.flip(dec.batch.q_idx, dims=[1]).contiguous()
+    dec_b = _gpu.decoder(ragged)
+    dec_b.batch.q.copy_(q_b)
+    dec_b.batch.q_idx.copy_(qi_b)
+    out_b, ids_b = (t.clone().cpu() for t in dec_b.decode())
+    torch.cuda.synchronize()
+    assert not torch.equal(out_a, out_b)
+    q_a, qi_a = dec.batch.q.cpu(), dec.batch.q_idx.cpu()
+    q_b, qi_b = q_b.cpu(), qi_b.cpu()
+    for depth in (1, 2, 3):
+        hs = dec.host_stream(depth)
+        got = {}
+
+        def fill(i, inp):
+            inp["q"].copy_(q_a if i % 2 == 0 else q_b)
+            inp["q_idx"].copy_(qi_a if i % 2 == 0 else qi_b)
+
+        def consume(i, res):
+            got[i] = (res["out"].clone(), res["block_ids"].clone(), res["lse"].clone())
+
+        hs.run(7, fill, consume)
+        assert sorted(got) == list(range(7))
+        for i, (o, ids, lse) in got.items():
+            if i % 2 == 0:
+                assert torch.equal(o, out_a) and torch.equal(ids, ids_a) and torch.equal(lse, lse_a), (depth, i)
+            else:
+                assert torch.equal(o, out_b) and torch.equal(ids, ids_b), (depth, i)
+
+
 @pytest.mark.parametrize("B", [1500, 2400])
 def test_many_requests(B):
     """Thousands of short requests: the scan's page prefix (one entry per request) lives in
