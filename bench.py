@@ -331,6 +331,15 @@ def measure_preset(name, l2_flush, stream, reps, peak):
            "query_rows": int(rows.sum()), "query_rows_per_s": round(float(rows.sum()) / step_s, 1),
            "step_bytes": sb["total"], "achieved_gbs": round(sb["total"] / step_s / 1e9, 1),
            "frac": round(sb["total"] / step_s / 1e9 / peak, 4), "reps": reps, "device_error_flags": flags}
+    ib = bm.distinct_index_bytes(wl.context_lens, rows, wl.block_table)
+    if ib["distinct"] < ib["logical"]:
+        # pages shared by several requests: the step's bytes with each shared page's index keys
+        # counted once (its K/V too are read from HBM once; the L2 serves the repeats)
+        uniq = sb["total"] - ib["logical"] + ib["distinct"]
+        out["shared_pages"] = {"index_bytes_logical": ib["logical"], "index_bytes_distinct": ib["distinct"],
+                               "logical_pages": ib["logical_pages"], "distinct_pages": ib["distinct_pages"],
+                               "step_bytes_distinct": uniq,
+                               "frac_distinct": round(uniq / step_s / 1e9 / peak, 4)}
     del dec, wl
     torch.cuda.empty_cache()
     return out

@@ -68,6 +68,28 @@ def step_bytes(context_lens, rows, block_ids=None, with_lse=True) -> dict:
     return {"index": index, "kv": kv, "queries": queries, "outputs": outputs, "meta": meta, "total": total}
 
 
+def distinct_index_bytes(context_lens, rows, block_table) -> dict:
+    """Index-key bytes of the active requests counted per logical block (what the scan
+    reads, `logical`) and per distinct physical page (`distinct`: a page that several
+    requests map, e.g. a common prompt prefix, counted once, with the most tokens any of them
+    uses). The difference is what reading each shared page once would save."""
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    bt = np.asarray(block_table)
+    tokens = {}
+    logical = 0
+    for b in np.nonzero(rows > 0)[0]:
+        n = int(ctx[b])
+        for c in range((n + BLOCK - 1) // BLOCK):
+            t = min(BLOCK, n - c * BLOCK)
+            logical += t
+            p = int(bt[b, c])
+            tokens[p] = max(tokens.get(p, 0), t)
+    distinct = sum(tokens.values())
+    return {"logical": logical * NVFP4_BYTES_PER_ROW, "distinct": distinct * NVFP4_BYTES_PER_ROW,
+            "logical_pages": int(sum((ctx[rows > 0] + BLOCK - 1) // BLOCK)), "distinct_pages": len(tokens)}
+
+
 def select_bytes(context_lens, rows) -> int:
     """Bytes the fused selection kernel must move: the index scan, the index
     queries, block-table entries and the block ids it writes."""

@@ -52,3 +52,26 @@ def test_step_bytes_of_the_128k_speculative_workload():
     assert r["kv"] == 16 * 4 * 2048 * 144
     assert r["queries"] == 128 * (4096 + 512)
     assert abs(r["total"] - 171.6e6) < 0.1e6
+
+
+def test_distinct_index_bytes_count_each_shared_page_once():
+    """A shared prefix of 4 pages over 3 requests: the logical count has every request's
+    pages, the distinct count the 4 prefix pages once; without sharing the two agree. A
+    request with no rows reads nothing."""
+    import numpy as np
+    from tests import _wl
+
+    ctx, rows = [1000, 2048, 600], [1, 2, 1]
+    wl = _wl.small(ctx, rows, shared=4, seed=3)
+    r = np.diff(wl.q_indptr)
+    got = bm.distinct_index_bytes(wl.context_lens, r, wl.block_table)
+    pages = [(n + 127) // 128 for n in ctx]                  # 8, 16, 5
+    assert got["logical_pages"] == sum(pages)
+    assert got["distinct_pages"] == sum(pages) - 2 * 4       # the prefix, once instead of 3 times
+    assert got["logical"] == sum(ctx) * 72
+    assert got["distinct"] == (sum(ctx) - 2 * 4 * 128) * 72  # the prefix pages are full in every request
+    own = _wl.small(ctx, rows, shared=0, seed=3)
+    got = bm.distinct_index_bytes(own.context_lens, np.diff(own.q_indptr), own.block_table)
+    assert got["distinct"] == got["logical"] == sum(ctx) * 72
+    got = bm.distinct_index_bytes(wl.context_lens, np.array([0, 2, 1]), wl.block_table)
+    assert got["logical"] == (2048 + 600) * 72 and got["distinct"] == (2048 + 600 - 4 * 128) * 72
