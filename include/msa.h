@@ -268,9 +268,13 @@ msa_status msa_dcp_merge_topk(const msa_decode_args* args, int32_t world, int32_
                               const uint64_t* all_keys, int32_t* block_ids, void* ws, size_t ws_bytes,
                               void* stream);
 
-/* The whole decode step: msa_select_blocks then msa_sparse_attn_decode, three
- * kernels on `stream`, each chained to the one before it with programmatic
- * dependent launch. */
+/* The whole decode step: the index scan with its block max pool, the top-k and the
+ * sparse attention on `stream`, each kernel chained to the one before it with
+ * programmatic dependent launch. The top-k runs in its own kernel (three kernels, as
+ * msa_select_blocks then msa_sparse_attn_decode), or inside the attention kernel (two
+ * kernels) when requests may exceed 1,025 blocks and each (request, group) is split over
+ * 4 or more attention CTAs, or when every (request, group) is one attention CTA and no
+ * request exceeds 1,025 blocks; the ids written are the same. */
 msa_status msa_decode(const msa_decode_args* args, int32_t* block_ids, uint16_t* out_bf16, float* lse,
                       void* ws, size_t ws_bytes, void* stream);
 
