@@ -19,9 +19,7 @@
 // over all four SM sub-partitions and a thread handles 128/C keys of its row:
 //   * load warp: one lane copies each block's raw NVFP4 K and V into a 4-stage
 //     shared-memory ring (codes by 2-D tensor copies with a 64-byte swizzle,
-//     scales by bulk copies) and, once the block ids are known, asks L2 to
-//     prefetch every later block of the split, so the ring refills from L2
-//     rather than waiting a full HBM round trip per stage;
+//     scales by bulk copies);
 //   * 8 dequant warps in two groups taking alternate blocks, thread = one K row
 //     and the same V row of the block: take the rows' codes into registers and
 //     release the raw stage at once, dequantise both in one interleaved pass to
@@ -65,7 +63,7 @@ namespace {
 constexpr int kSoftWarps = 8;                       // warps 0..7: two sets of 4, one per TMEM lane quadrant
 constexpr int kMmaWarp = 8;                         // S = Q K^T issue, TMEM allocation
 constexpr int kPvWarp0 = 9;                         // warps 9, 10: O_s += P V issue for set s
-constexpr int kLoadWarp = 11;                       // raw page copies, L2 prefetch
+constexpr int kLoadWarp = 11;                       // raw page copies
 constexpr int kDqWarp0 = 12, kDqWarps = 8;          // warps 12..19: two groups of 4
 constexpr int kAttnThreads = (kDqWarp0 + kDqWarps) * 32;
 // raw NVFP4 page ring: two stages per dequant group (the groups take alternate blocks), so
@@ -380,16 +378,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       int issued = 0;
       for (; issued < nmy && issued < kAttnStages; ++issued) issue(issued);
-      // every later block of the split into L2 now: its stage then fills from L2
-      for (int j = kAttnStages; j < nmy; ++j) {
-        const int phys = sm.phys[jb0 + j];
-        if (page_bad(phys)) continue;
-        const long long head_row = (static_cast<long long>(phys) * kGroups + g) * kBlock;
-        prefetch_l2(p.k_data + head_row * 64, kHeadPageBytes);
-        prefetch_l2(p.v_data + head_row * 64, kHeadPageBytes);
-        prefetch_l2(p.k_scale + head_row * 8, kHeadScaleBytes);
-        prefetch_l2(p.v_scale + head_row * 8, kHeadScaleBytes);
-      }
+      // (no L2 prefetch of the later blocks: with a 4-stage ring the copies keep up, and
+      // asking L2 for every later block at once was measured ~1-2.6 us slower per call on
+      // GB300 at 8 and 16 blocks per CTA)
       for (; issued < nmy; ++issued) {
         const int st = raw_stage(issued);
         if (!wait_bar(smem_u32(&sm.raw_empty[st]), ((issued / kAttnStages) - 1) & 1, p.flags)) break;
