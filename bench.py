@@ -524,6 +524,8 @@ def run_libmsa(args, rank, world, dist):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": dict(workload_config(args.workload, spec, "flushed before every timed step (512 MiB write, then read back)"),
+                           l2_e2e="e2e: not flushed between steps; inputs larger than L2 (171.6 MB per step > "
+                                  "129 MB); e2e.serial: flushed before every step",
                            parallelism=f"replicas x{world}"),
             "step_time": spread(step_ms),
             "step_bytes": step_bytes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
