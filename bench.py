@@ -492,7 +492,7 @@ def run_libmsa(args, rank, world, dist):
            "path": "MSADecoder.host_stream(3).run(): per step 1 H2D copy, 3 kernels, 1 D2H copy and a host read "
                    "of the result; three steps in flight (each slot its own buffers), copies on two copy streams, "
                    "the kernels of all steps on one compute stream",
-           "l2": "not flushed between steps (171.6 MB of inputs per step > 129 MB L2)",
+           "l2": f"not flushed between steps ({step_bytes['total'] / 1e6:.1f} MB moved per step; L2 129 MB)",
            "serial": serial}
 
     # ---- CPU baseline: the oracle as it stands, rank 0 only, bounded sample, at all the
@@ -524,8 +524,8 @@ def run_libmsa(args, rank, world, dist):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": dict(workload_config(args.workload, spec, "flushed before every timed step (512 MiB write, then read back)"),
-                           l2_e2e="e2e: not flushed between steps; inputs larger than L2 (171.6 MB per step > "
-                                  "129 MB); e2e.serial: flushed before every step",
+                           l2_e2e=f"e2e: not flushed between steps ({step_bytes['total'] / 1e6:.1f} MB moved per "
+                                  "step; L2 129 MB); e2e.serial: flushed before every step",
                            parallelism=f"replicas x{world}"),
             "step_time": spread(step_ms),
             "step_bytes": step_bytes, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
